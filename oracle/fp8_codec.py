@@ -1,0 +1,58 @@
+"""FP8 latent-cache decoding, written from the published format definitions.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Format facts used:
+  * "DeepSeek-R1" model record, engine kernel constraint (2): latents are
+    stored as float8_e4m3 with one float8_e8m0 scale per 32 e4m3 values,
+    inlined in each token's row.
+  * "DeepSeek R1 Architecture & Deployment Guide", section 4: E4M3 max
+    normal = 448.0.
+  * OCP 8-bit floating point specification, E4M3 ("fn" flavour): 1 sign bit,
+    4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes
+    subnormals m/8 * 2^-6; no infinities; S.1111.111 is NaN.
+  * OCP Microscaling (MX) specification, E8M0 scale: an unsigned 8-bit
+    exponent with bias 127, value 2^(e-127); 0xFF is NaN.
+
+Row layout (the reading taken for the 594-byte row): bytes [0, 576) are the
+e4m3 codes of the 576 values (512 latent, then 64 RoPE), bytes [576, 594) are
+18 e8m0 scales, scale k covering values [32k, 32k+32).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ROW_VALUES = 576
+SCALE_GROUP = 32
+NUM_SCALES = ROW_VALUES // SCALE_GROUP
+ROW_BYTES = ROW_VALUES + NUM_SCALES
+
+
+def e4m3fn_to_float64(codes: np.ndarray) -> np.ndarray:
+    """Decode OCP E4M3FN bytes to float64 by their bit fields."""
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((b & 0x80) != 0, -1.0, 1.0)
+    exp = (b >> 3) & 0xF
+    man = (b & 0x7).astype(np.float64)
+    normal = sign * (1.0 + man / 8.0) * np.exp2(exp - 7)
+    subnormal = sign * (man / 8.0) * 2.0 ** -6
+    val = np.where(exp == 0, subnormal, normal)
+    return np.where((exp == 0xF) & ((b & 0x7) == 0x7), np.nan, val)
+
+
+def e8m0_to_float64(codes: np.ndarray) -> np.ndarray:
+    """Decode OCP MX E8M0 scale bytes: 2^(e-127), 0xFF -> NaN."""
+    e = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return np.where(e == 0xFF, np.nan, np.exp2(e - 127).astype(np.float64))
+
+
+def dequant_rows(raw: np.ndarray) -> np.ndarray:
+    """[..., 594] uint8 rows -> [..., 576] float64 values.
+
+    value[k] = e4m3(byte[k]) * e8m0(byte[576 + k // 32]).
+    """
+    raw = np.asarray(raw, dtype=np.uint8)
+    assert raw.shape[-1] == ROW_BYTES, raw.shape
+    vals = e4m3fn_to_float64(raw[..., :ROW_VALUES])
+    scales = e8m0_to_float64(raw[..., ROW_VALUES:])
+    return vals * np.repeat(scales, SCALE_GROUP, axis=-1)

@@ -1,0 +1,51 @@
+"""The seeded input generator: determinism and the structure of the five workloads."""
+import torch
+
+from mla_latent_kv_05_gb300 import inputs as gen
+
+
+def test_same_seed_same_inputs():
+    a = gen.make_inputs(3, 2, [5, 64, 130], seed=4)
+    b = gen.make_inputs(3, 2, [5, 64, 130], seed=4)
+    for x, y in [(a.q_absorbed, b.q_absorbed), (a.q_rope, b.q_rope), (a.kv_cache, b.kv_cache),
+                 (a.block_table, b.block_table), (a.seq_lens, b.seq_lens)]:
+        assert torch.equal(x, y)
+    c = gen.make_inputs(3, 2, [5, 64, 130], seed=5)
+    assert not torch.equal(a.kv_cache, c.kv_cache)
+
+
+def test_block_table_is_a_slice_of_a_permutation():
+    inp = gen.make_inputs(4, 1, [1, 64, 65, 0], seed=2, physical_pages=10)
+    bt = inp.block_table
+    used = []
+    for b, s in enumerate(inp.seq_lens.tolist()):
+        n = (s + 63) // 64
+        used += bt[b, :n].tolist()
+        assert torch.all(bt[b, n:] == -1)
+    assert len(set(used)) == len(used) == 4
+    assert all(0 <= p < inp.num_pages for p in used)
+
+
+def test_workload_shapes():
+    seq3 = gen.workload_seq_lens(3)
+    assert len(seq3) == 64 and min(seq3) >= 1 and max(seq3) <= 32768
+    assert seq3 == gen.workload_seq_lens(3)
+    assert gen.workload_seq_lens(5) == [131072] * 4
+    w1 = gen.make_workload(1)
+    assert w1.kv_cache.shape == (8, 64, 576) and w1.kv_cache.dtype == torch.bfloat16
+    assert w1.q_absorbed.shape == (1, 1, 128, 512) and w1.q_rope.shape == (1, 1, 128, 64)
+
+
+def test_fp8_scale_bytes_in_range():
+    inp = gen.make_inputs(2, 1, [100, 3], kv_dtype="fp8", seed=1)
+    assert inp.kv_cache.shape[-1] == 594 and inp.kv_cache.dtype == torch.uint8
+    sc = inp.kv_cache[..., 576:]
+    assert int(sc.min()) >= 120 and int(sc.max()) <= 130
+    vals = inp.kv_cache[..., :576].contiguous().view(torch.float8_e4m3fn).float()
+    assert torch.isfinite(vals).all()
+
+
+def test_counts_workload2():
+    c = gen.workload_counts(gen.make_inputs(32, 1, [4096] * 32, seed=0, num_heads=128))
+    assert c["kv_tokens"] == 32 * 4096
+    assert c["flops"] == 32 * 4096 * 2 * 128 * (576 + 512)

@@ -1,0 +1,306 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Closed forms printed on the pages, torch's float8 casts, torch's float64
+scaled-dot-product attention, the matrix-absorption identity (two independent
+computations), brute-force special cases and invariants.  The last test
+plants plausible mistakes in copies of the oracle and checks that each is
+caught by at least one pin.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import closed_forms as cf
+from oracle import fp8_codec, mla_oracle
+from mla_latent_kv_05_gb300 import inputs as gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_forms.txt")
+
+
+def _golden():
+    out = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, value, tol, _where = [x.strip() for x in line.split("|", 3)]
+        out[name] = (float(value), float(tol))
+    return out
+
+
+def test_closed_forms_match_printed_values():
+    g = _golden()
+    computed = {
+        "mla_elems_per_token_layer": cf.mla_elems_per_token_layer(),
+        "mla_bytes_per_token_61_layers_bf16": cf.mla_bytes_per_token(),
+        "mla_kib_per_token_61_layers_bf16": cf.mla_bytes_per_token() / 1024,
+        "mla_cache_gb_128k_bf16": cf.mla_cache_bytes() / 1e9,
+        "mha_cache_gb_128k_bf16": cf.mha_cache_bytes() / 1e9,
+        "mla_reduction_vs_mha_percent": 100 * cf.mla_reduction_vs_mha(),
+        "mha_elems_per_token_layer": cf.mha_elems_per_token_layer(),
+        "e4m3_max_normal": float(np.nanmax(fp8_codec.e4m3fn_to_float64(np.arange(256, dtype=np.uint8)))),
+        "fp8_scales_per_row_group": fp8_codec.SCALE_GROUP,
+        "page_block_size": cf.PAGE_SIZE,
+    }
+    assert set(computed) == set(g)
+    for k, (v, tol) in g.items():
+        assert abs(computed[k] - v) <= tol + 1e-12, (k, computed[k], v)
+    # exact integers behind the printed figures
+    assert cf.mla_cache_bytes() == 9_210_691_584
+    assert cf.mha_cache_bytes() == 523_986_010_112
+    assert cf.fp8_row_bytes() == 594 and cf.fp8_page_bytes() == 38_016
+
+
+def test_e4m3_table_matches_torch_cast():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = fp8_codec.e4m3fn_to_float64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.isnan(mine).sum() == 2           # 0x7F and 0xFF only
+    assert mine[0x7E] == 448.0 and mine[0xFE] == -448.0
+    assert mine[0x01] == 2.0 ** -9             # smallest subnormal
+
+
+def test_e8m0_matches_torch_cast():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = fp8_codec.e8m0_to_float64(codes)
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch has no float8_e8m0fnu")
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_fp8_row_dequant_layout_against_torch():
+    inp = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp8", seed=3)
+    raw = inp.kv_cache
+    mine = fp8_codec.dequant_rows(raw.numpy())
+    v = raw[..., :576].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    s = raw[..., 576:].contiguous().view(torch.float8_e8m0fnu).to(torch.float64)
+    ref = (v * s.repeat_interleave(32, dim=-1)).numpy()
+    assert np.array_equal(mine, ref)
+    # every dequantised value is exactly representable in bf16
+    as_bf16 = torch.from_numpy(mine).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(as_bf16, mine)
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def _sdpa_reference(q_abs, q_rope, rows, scale):
+    """torch's float64 SDPA on the gathered dense keys; lse by torch.logsumexp."""
+    q = torch.cat([torch.from_numpy(q_abs), torch.from_numpy(q_rope)], -1)[None, :, None, :]  # [1, H, 1, 576]
+    k = torch.from_numpy(rows)[None, None, :, :].expand(1, q.shape[1], -1, -1)
+    v = torch.from_numpy(rows[:, :512])[None, None, :, :].expand(1, q.shape[1], -1, -1)
+    out = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale)
+    lse = torch.logsumexp(scale * (q @ k.transpose(-1, -2)), dim=-1)
+    return out[0, :, 0].numpy(), lse[0, :, 0].numpy()
+
+
+def _gathered(inp, b, i=0):
+    rows = mla_oracle.cache_rows(_f64(inp.kv_cache) if inp.kv_dtype == "bf16" else inp.kv_cache.numpy(), inp.kv_dtype)
+    n = max(mla_oracle.visible_len(int(inp.seq_lens[b]), inp.sq, i), 0)
+    return mla_oracle.gather_rows(rows, inp.block_table[b].numpy(), n)
+
+
+@pytest.mark.parametrize("seq,kv", [([256], "bf16"), ([1, 63, 64, 65, 200], "bf16"), ([130, 7], "fp8")])
+def test_attend_matches_torch_sdpa(seq, kv):
+    inp = gen.make_inputs(len(seq), 1, seq, kv_dtype=kv, seed=11)
+    for b in range(len(seq)):
+        g = _gathered(inp, b)
+        out, lse = mla_oracle.attend_latent(_f64(inp.q_absorbed[b, 0]), _f64(inp.q_rope[b, 0]), g, inp.scale)
+        ro, rl = _sdpa_reference(_f64(inp.q_absorbed[b, 0]), _f64(inp.q_rope[b, 0]), g, inp.scale)
+        np.testing.assert_allclose(out, ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse, rl, rtol=1e-12, atol=1e-12)
+
+
+def test_workload1_matches_sdpa():
+    inp = gen.make_workload(1)
+    assert inp.num_pages == 8 and inp.max_pages == 4 and int(inp.seq_lens[0]) == 256
+    rows = mla_oracle.cache_rows(_f64(inp.kv_cache), "bf16")
+    out, lse = mla_oracle.mla_decode(_f64(inp.q_absorbed), _f64(inp.q_rope), rows,
+                                     inp.block_table.numpy(), inp.seq_lens.numpy(), inp.scale)
+    ro, rl = _sdpa_reference(_f64(inp.q_absorbed[0, 0]), _f64(inp.q_rope[0, 0]), _gathered(inp, 0), inp.scale)
+    np.testing.assert_allclose(out[0, 0], ro, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], rl, rtol=1e-12)
+
+
+def test_absorption_identity():
+    """Un-absorbed attention with explicit W^UK / W^UV equals the absorbed
+    latent form followed by W^UV (architecture guide, section 1.1)."""
+    rng = np.random.default_rng(5)
+    H, d_h, n = 16, 128, 97
+    w_uk = rng.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    w_uv = rng.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    q_nope = rng.standard_normal((H, d_h))
+    q_rope = rng.standard_normal((H, 64))
+    c_kv = rng.standard_normal((n, 512))
+    k_r = rng.standard_normal((n, 64))
+    scale = 1 / math.sqrt(192)
+    o_ref, lse_ref = mla_oracle.attend_unabsorbed(q_nope, q_rope, c_kv, k_r, w_uk, w_uv, scale)
+    q_abs = mla_oracle.absorb_query(q_nope, w_uk)
+    out_lat, lse = mla_oracle.attend_latent(q_abs, q_rope, np.concatenate([c_kv, k_r], 1), scale)
+    o = mla_oracle.up_project_output(out_lat, w_uv)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12)
+
+
+def test_single_token_is_exact_row():
+    rng = np.random.default_rng(1)
+    row = rng.standard_normal((1, 576))
+    qa, qr = rng.standard_normal((128, 512)), rng.standard_normal((128, 64))
+    out, lse = mla_oracle.attend_latent(qa, qr, row, 0.1)
+    assert np.array_equal(out, np.broadcast_to(row[0, :512], (128, 512)))
+    np.testing.assert_allclose(lse, 0.1 * (qa @ row[0, :512] + qr @ row[0, 512:]), rtol=1e-13)
+
+
+def test_identical_rows_mean_and_log_n():
+    rng = np.random.default_rng(2)
+    row = rng.standard_normal(576)
+    n = 37
+    rows = np.tile(row, (n, 1))
+    qa, qr = rng.standard_normal((128, 512)), rng.standard_normal((128, 64))
+    out, lse = mla_oracle.attend_latent(qa, qr, rows, 0.05)
+    np.testing.assert_allclose(out, np.broadcast_to(row[:512], (128, 512)), rtol=1e-13, atol=1e-14)
+    s = 0.05 * (qa @ row[:512] + qr @ row[512:])
+    np.testing.assert_allclose(lse, s + math.log(n), rtol=1e-13)
+
+
+def test_dominant_score_selects_row():
+    rng = np.random.default_rng(3)
+    rows = rng.standard_normal((20, 576)) * 0.01
+    qa = np.zeros((1, 512)); qr = np.zeros((1, 64))
+    qa[0, 7] = 1.0
+    rows[13, 7] = 50.0
+    out, _ = mla_oracle.attend_latent(qa, qr, rows, 1.0)
+    np.testing.assert_allclose(out[0], rows[13, :512], atol=1e-15 * 1e6)
+
+
+def test_page_permutation_invariance_and_unused_slots():
+    inp = gen.make_inputs(3, 1, [100, 64, 129], seed=8, physical_pages=9)
+    rows = mla_oracle.cache_rows(_f64(inp.kv_cache), "bf16")
+    qa, qr = _f64(inp.q_absorbed), _f64(inp.q_rope)
+    bt, sl = inp.block_table.numpy(), inp.seq_lens.numpy()
+    out, lse = mla_oracle.mla_decode(qa, qr, rows, bt, sl, inp.scale)
+    perm = np.random.default_rng(0).permutation(rows.shape[0])
+    inv = np.argsort(perm)
+    rows2 = rows[perm].copy()
+    bt2 = np.where(bt >= 0, inv[np.maximum(bt, 0)], -1)
+    # slots past the visible length hold garbage, which must not matter
+    for b, s in enumerate(sl):
+        if s % 64:
+            rows2[bt2[b, s // 64], s % 64:] = np.nan
+    out2, lse2 = mla_oracle.mla_decode(qa, qr, rows2, bt2, sl, inp.scale)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_split_merge_equals_unsplit():
+    rng = np.random.default_rng(4)
+    rows = rng.standard_normal((300, 576))
+    qa, qr = rng.standard_normal((128, 512)), rng.standard_normal((128, 64))
+    full, lse_full = mla_oracle.attend_latent(qa, qr, rows, 0.07)
+    for cuts in ([0, 150, 300], [0, 1, 64, 65, 299, 300], [0, 299, 300]):
+        parts = [mla_oracle.attend_latent(qa, qr, rows[a:b], 0.07) for a, b in zip(cuts[:-1], cuts[1:])]
+        o, l = mla_oracle.merge_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        np.testing.assert_allclose(o, full, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(l, lse_full, rtol=1e-13)
+    # an empty part (lse = -inf) contributes nothing
+    e = mla_oracle.attend_latent(qa, qr, rows[:0], 0.07)
+    o, l = mla_oracle.merge_partials(np.stack([full, e[0]]), np.stack([lse_full, e[1]]))
+    np.testing.assert_allclose(o, full, rtol=1e-13)
+
+
+def test_causal_two_token_query():
+    inp = gen.make_inputs(2, 2, [65, 1], seed=9)
+    rows = mla_oracle.cache_rows(_f64(inp.kv_cache), "bf16")
+    qa, qr = _f64(inp.q_absorbed), _f64(inp.q_rope)
+    out, lse = mla_oracle.mla_decode(qa, qr, rows, inp.block_table.numpy(), inp.seq_lens.numpy(), inp.scale)
+    for b, s in enumerate([65, 1]):
+        for i, n in enumerate([s - 1, s]):
+            g = mla_oracle.gather_rows(rows, inp.block_table[b].numpy(), n)
+            if n == 0:
+                assert np.all(out[b, i] == 0) and np.all(lse[b, i] == -np.inf)
+                continue
+            ro, rl = _sdpa_reference(qa[b, i], qr[b, i], g, inp.scale)
+            np.testing.assert_allclose(out[b, i], ro, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(lse[b, i], rl, rtol=1e-12)
+
+
+def _pin_suite(attend):
+    """Run the attention pins against a candidate implementation; return the
+    number of pins that fail."""
+    fails = 0
+    rng = np.random.default_rng(12)
+    rows = rng.standard_normal((70, 576))
+    qa, qr = rng.standard_normal((8, 512)), rng.standard_normal((8, 64))
+    try:
+        o, l = attend(qa, qr, rows, 0.07)
+        ro, rl = _sdpa_reference(qa, qr, rows, 0.07)
+        if not (np.allclose(o, ro, rtol=1e-10) and np.allclose(l, rl, rtol=1e-10)):
+            fails += 1
+    except Exception:
+        fails += 1
+    o, l = attend(qa, qr, rows[:1], 0.07)
+    if not np.allclose(o, np.broadcast_to(rows[0, :512], o.shape)):
+        fails += 1
+    return fails
+
+
+def test_planted_mistakes_are_caught():
+    good = mla_oracle.attend_latent
+
+    def no_rope(qa, qr, rows, sc):
+        return good(qa, np.zeros_like(qr), rows, sc)
+
+    def scale_outside(qa, qr, rows, sc):
+        o, l = good(qa, qr, rows, 1.0)
+        return o, l * sc
+
+    def v_includes_rope_slice(qa, qr, rows, sc):
+        shifted = np.concatenate([rows[:, 64:], rows[:, :64]], 1)
+        o, l = good(qa, qr, rows, sc)
+        o2, _ = good(qa, qr, shifted, sc)
+        return o2, l
+
+    def off_by_one_len(qa, qr, rows, sc):
+        return good(qa, qr, rows[:-1] if rows.shape[0] > 1 else rows, sc)
+
+    assert _pin_suite(good) == 0
+    for bad in (no_rope, scale_outside, v_includes_rope_slice, off_by_one_len):
+        assert _pin_suite(bad) >= 1, bad.__name__
+
+    # a wrong page or slot index is caught by the marker pin
+    def bad_gather(rows, btr, n):
+        j = np.arange(int(n))
+        return rows[np.asarray(btr)[j // rows.shape[1]], (j + 1) % rows.shape[1]]
+
+    assert _marker_gather_ok(mla_oracle.gather_rows)
+    assert not _marker_gather_ok(bad_gather)
+
+
+def _marker_gather_ok(gather):
+    """Fill every physical slot with the token index the block table says it
+    holds (and -1 in unused slots); gathering must return 0, 1, ..., n-1."""
+    inp = gen.make_inputs(3, 1, [100, 64, 129], seed=8, physical_pages=9)
+    bt, sl = inp.block_table.numpy(), inp.seq_lens.numpy()
+    rows = np.full((inp.num_pages, 64, 576), -1.0)
+    for b, s in enumerate(sl):
+        for j in range(s):
+            rows[bt[b, j // 64], j % 64, :] = j
+    for b, s in enumerate(sl):
+        g = gather(rows, bt[b], s)
+        if not np.array_equal(g[:, 0], np.arange(s)) or not np.all(g == g[:, :1]):
+            return False
+    return True
+
+
+def test_gather_by_markers():
+    assert _marker_gather_ok(mla_oracle.gather_rows)
