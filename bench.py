@@ -1,0 +1,408 @@
+"""Benchmark: MLA decode over a paged latent KV cache on GB300.
+
+One step = one full decode call through the C ABI (split-KV planner, paired
+tcgen05 attention kernel, LSE merge) over one batch of synthetic inputs that
+are already resident in HBM.  Default workload: batch 64, Sq 1, seq_lens
+drawn uniformly in [1, 32768] (seed 1003), bf16 cache with shuffled pages.
+
+Printed (one JSON line): KV-tokens/s of the whole job, ms/step, the
+roofline record of the attention kernel (timed alone with CUDA events on its
+stream), an end-to-end number through the public API with host buffers, the
+float64 oracle timed on the host cores on a bounded sample, and the SM
+clocks sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+  python bench.py --impl reference ...   # the oracle arm (host cores)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mla_latent_kv_05_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MLA decode KV-tokens/s, HBM GB/s & TFLOP/s vs 1xGB300 roofline; us/call"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: int, kind: str):
+    """DRAM bytes per launch of the attention kernel from a committed ncu
+    summary, only if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "decode_dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(f"{kind}:{workload}")
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        smax = max(r["smax"] for r in rows)
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                          ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in loaded):
+                reasons.append(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in loaded])), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_sample(inp, budget_s: float, max_tokens_per_piece: int = 4096):
+    """Time the float64 oracle (as it stands) on a bounded sample of the
+    workload: whole (row, query) attentions over the first rows, each cut to
+    at most `max_tokens_per_piece` tokens, until `budget_s` elapses.
+    Returns (KV tokens processed, seconds, description)."""
+    from oracle import mla_oracle
+    raw = inp.kv_cache if inp.kv_dtype == "fp8" else inp.kv_cache
+    qa = inp.q_absorbed
+    qr = inp.q_rope
+    tokens = 0
+    t0 = time.perf_counter()
+    pieces = 0
+    b = 0
+    while time.perf_counter() - t0 < budget_s:
+        bb = b % inp.batch
+        n = min(int(inp.seq_lens[bb]), max_tokens_per_piece)
+        if n > 0:
+            pages = inp.block_table[bb, : (n + 63) // 64].long()
+            sub = raw[pages]
+            rows = mla_oracle.cache_rows(sub.numpy() if inp.kv_dtype == "fp8" else sub.double().numpy(),
+                                         inp.kv_dtype)
+            local_bt = np.arange(len(pages))
+            g = mla_oracle.gather_rows(rows, local_bt, n)
+            for i in range(inp.sq):
+                mla_oracle.attend_latent(qa[bb, i].double().numpy(), qr[bb, i].double().numpy(), g, inp.scale)
+            tokens += n
+            pieces += 1
+        b += 1
+    dt = time.perf_counter() - t0
+    return tokens, dt, f"{pieces} (row, all queries) attentions of <= {max_tokens_per_piece} tokens, 128 heads"
+
+
+def run_reference(args):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return 0
+    inp = gen.make_workload(args.workload)
+    cfg = workload_config(args.workload, inp)
+    per_step = 0.01
+    for _ in range(args.warmup):
+        oracle_sample(inp, per_step)
+    tot_tok, tot_s = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        t, s, desc = oracle_sample(inp, per_step)
+        tot_tok += t
+        tot_s += s
+    value = tot_tok / tot_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "KV-tokens/s", "cores": _CORES, "kind": "oracle",
+                         "sample": f"per step: {desc}; ~{per_step}s of host work"},
+        "e2e": {"value": value, "unit": "KV-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def workload_config(workload: int, inp) -> dict:
+    c = gen.workload_counts(inp)
+    return {"workload": gen.WORKLOADS[workload]["name"], "batch": inp.batch, "sq": inp.sq,
+            "heads": int(inp.q_absorbed.shape[2]), "kv_dtype": inp.kv_dtype, "page_size": 64,
+            "kv_tokens": c["kv_tokens"], "seed": gen.seed_for(workload),
+            "l2": "inputs larger than L2 (KV cache %.0f MB > 129 MB)" % (c["kv_bytes"] / 1e6)
+            if c["kv_bytes"] > L2_BYTES else "L2 flushed between steps"}
+
+
+def run_ours(args):
+    from mla_latent_kv_05_gb300 import binding
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = gen.make_workload(args.workload)
+    counts = gen.workload_counts(inp)
+    decode = binding.mla_decode_bf16 if inp.kv_dtype == "bf16" else binding.mla_decode_fp8
+    q = inp.q_absorbed.to(dev)
+    qr = inp.q_rope.to(dev)
+    kv = inp.kv_cache.to(dev)
+    bt = inp.block_table.to(dev)
+    sl = inp.seq_lens.to(dev)
+    out = torch.empty((inp.batch, inp.sq, 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((inp.batch, inp.sq, 128), dtype=torch.float32, device=dev)
+    ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = None
+    if counts["kv_bytes"] <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        decode(q, qr, kv, bt, sl, inp.scale, out=out, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    st = binding.mla_get_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {binding.status_string(st)}")
+
+    # ---- timed region: K whole steps, barrier + sync on both sides
+    kern_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    for a, b in kern_ev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t_start = time.perf_counter()
+        for k in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            step_ev[k][0].record(stream)
+            binding.mla_profile_next_decode(*kern_ev[k])
+            step()
+            step_ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        wall = time.perf_counter() - t_start
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kern_ev]
+    st = binding.mla_get_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {binding.status_string(st)}")
+    total_ms = float(np.sum(step_ms))
+    total_ms_max = max_over_ranks(total_ms, world, dev)
+    tokens_all = sum_over_ranks(float(counts["kv_tokens"] * args.steps), world, dev)
+    value = tokens_all / (total_ms_max / 1000.0)
+    ms_per_step = total_ms_max / args.steps
+
+    # ---- roofline of the attention kernel
+    peaks = load_peaks()
+    kern_s = float(np.mean(kern_ms)) / 1000.0
+    bytes_alg = counts["bytes"]
+    flops = counts["flops"]
+    gbs = bytes_alg / kern_s / 1e9
+    tfs = flops / kern_s / 1e12
+    t_bytes = bytes_alg / (peaks["hbm"] * 1e9)
+    t_flop = flops / (peaks["bf16"] * 1e12)
+    if t_bytes >= t_flop:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": tfs / peaks["bf16"]}
+    roof["traffic"] = recorded_traffic(args.workload, inp.kv_dtype)
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
+    roof["kernel_us"] = kern_s * 1e6
+    roof["roofline_us"] = max(t_bytes, t_flop) * 1e6
+    roof["roofline_frac_of_call"] = max(t_bytes, t_flop) / (ms_per_step / 1000.0)
+    roof["hbm_gbs"] = gbs
+    roof["tflops"] = tfs
+
+    # ---- end to end through the public API with pinned host buffers
+    hq = inp.q_absorbed.pin_memory()
+    hqr = inp.q_rope.pin_memory()
+    hbt = inp.block_table.pin_memory()
+    hsl = inp.seq_lens.pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        qr.copy_(hqr, non_blocking=True)
+        bt.copy_(hbt, non_blocking=True)
+        sl.copy_(hsl, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = sum_over_ranks(float(counts["kv_tokens"] * e2e_steps), world, dev) / (e2e_ms / 1000.0)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hqr, hbt, hsl))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_call": ms_per_step * 1000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": inp.kv_dtype,
+        "data": "synthetic", "config": workload_config(args.workload, inp),
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "KV-tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "q, q_rope, block_table, seq_lens uploaded and out, lse read back every step; "
+                        "the KV cache stays resident in HBM"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tok, sec, desc = oracle_sample(inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tok / sec, "unit": "KV-tokens/s", "cores": _CORES, "kind": "oracle",
+                                "sample": f"{desc}; {sec:.1f}s of host work"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

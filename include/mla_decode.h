@@ -1,0 +1,131 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * Multi-Head Latent Attention decode over a paged compressed-latent KV cache
+ * ("DeepSeek R1 Architecture & Deployment Guide", section 1.1, matrix
+ * absorption and decoupled RoPE).  Each cached token is one row
+ * [c_KV (512) | k_R (64)] = 576 values.  The 128 query heads arrive absorbed:
+ * q_absorbed = (W^UK)^T q (512 values) and q_rope (64 values, already
+ * rotated).  For every query row and head h the library computes
+ *
+ *     s_j   = scale * (q_absorbed[h] . c_KV_j + q_rope[h] . k_R_j)
+ *     out[h]= sum_j softmax_j(s) * c_KV_j            (512 values, latent space)
+ *     lse[h]= ln sum_j exp(s_j)                      (natural log, scale included)
+ *
+ * V is the latent c_KV itself (W^UV is folded into the output projection,
+ * same section); k_R enters the scores only.
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *   q_absorbed  [B, Sq, 128, 512] bf16      q_rope [B, Sq, 128, 64] bf16
+ *   kv_cache    bf16: [num_pages, 64, 576]  (1152 B per token)
+ *               fp8 : [num_pages, 64, 594] bytes: 576 e4m3 codes then 18
+ *                     e8m0 scales, scale k covering values [32k, 32k+32)
+ *                     (inlined per-token scales, "DeepSeek-R1" model record,
+ *                     engine kernel constraint (2); 16-byte aligned base)
+ *   block_table [B, max_pages] int32: page p_index of row b; token t of row
+ *               b is page block_table[b][t/64], slot t%64 (page-block size
+ *               64, same record, constraint (1)).  Entries past
+ *               ceil(seq_len/64) are never read.
+ *   seq_lens    [B] int32, 0 <= seq_len <= max_pages*64.
+ *   out         [B, Sq, 128, 512] bf16      lse [B, Sq, 128] fp32
+ *
+ * Speculative multi-token queries (Multi-Token Prediction, guide section 4):
+ * query i of Sq sees the first seq_len - (Sq-1-i) tokens.  A query row that
+ * sees no token gets out = 0 and lse = -inf.
+ *
+ * Ownership: the caller owns every buffer; the library never allocates,
+ * frees or synchronises inside the decode calls.  All work is queued on
+ * `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
+ * Tokens past seq_len inside a row's last page are ignored whatever they
+ * hold (including NaN).
+ *
+ * Errors: host-side validation failures return a negative mla_status before
+ * anything is launched.  Launch failures return MLA_ERR_CUDA.  Problems only
+ * the device can see (a block-table entry outside [0, num_pages), a
+ * seq_len outside [0, max_pages*64], an internal wait that timed out) are
+ * recorded in a status word inside the workspace, read by mla_get_status.
+ * A bad page is never read: its rows are taken as zeros.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad alignment  */
+  MLA_ERR_UNSUPPORTED = -2,   /* num_heads != 128, page_size != 64, Sq > 4   */
+  MLA_ERR_WORKSPACE = -3,     /* workspace too small                          */
+  MLA_ERR_CUDA = -4,          /* a CUDA runtime call failed                   */
+  MLA_STATUS_BAD_PAGE = -5,   /* device: block-table entry out of range       */
+  MLA_STATUS_TIMEOUT = -6,    /* device: a pipeline wait gave up              */
+  MLA_STATUS_BAD_SEQ_LEN = -7 /* device: seq_len outside [0, max_pages*64]    */
+} mla_status;
+
+/* Bytes of device workspace a decode call with these sizes needs on the
+ * current device (the split-KV plan, per-split partial outputs and the
+ * status word).  Returns MLA_OK and writes *bytes, or a negative status. */
+int mla_workspace_size(int batch, int sq, int num_heads, int page_size, size_t* bytes);
+
+/* MLA decode over a bf16 latent cache (guide section 1.1; see top of file).
+ * Queues: the split-KV planner, the paired tcgen05 decode kernel and the
+ * LSE-merge kernel.  workspace: device memory of at least
+ * mla_workspace_size(...) bytes, 256-byte aligned, not shared with a call
+ * that may run concurrently.  Returns MLA_OK or a negative mla_status. */
+int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                    const uint16_t* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, int batch, int sq, int num_heads,
+                    int num_pages, int page_size, int max_pages,
+                    float softmax_scale, uint16_t* out, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same over the FP8 cache: each 594-byte row is dequantised as
+ * v[k] = e4m3(byte[k]) * 2^(byte[576 + k/32] - 127) ("DeepSeek-R1" model
+ * record, engine kernel constraint (2): e4m3 values, one e8m0 scale per 32)
+ * and then attended exactly as the bf16 path (the dequantised values are
+ * exact in bf16).  kv_cache must be 16-byte aligned. */
+int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                   const uint8_t* kv_cache, const int32_t* block_table,
+                   const int32_t* seq_lens, int batch, int sq, int num_heads,
+                   int num_pages, int page_size, int max_pages,
+                   float softmax_scale, uint16_t* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Merge split-KV partial results (attention over disjoint token sets):
+ *   L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * partial_out_s,
+ *   lse = L.
+ * partial_out [n_parts, num_heads, 512] fp32 (each part already normalised
+ * by its own softmax sum), partial_lse [n_parts, num_heads] fp32,
+ * split_indptr [rows+1] int32: row r merges parts [indptr[r], indptr[r+1]).
+ * A row with no part (or whose parts all have lse = -inf) gets out = 0,
+ * lse = -inf.  out [rows, num_heads, 512] bf16, lse [rows, num_heads] fp32.
+ * num_heads must be 128. */
+int mla_combine_splits(const float* partial_out, const float* partial_lse,
+                       const int32_t* split_indptr, int rows, int num_heads,
+                       uint16_t* out, float* lse, void* stream);
+
+/* Synchronises `stream`, then returns the device status word recorded in
+ * `workspace` by the calls queued before (MLA_OK or an MLA_STATUS_* code)
+ * and clears it.  Returns MLA_ERR_CUDA if the stream reported an error. */
+int mla_get_status(void* workspace, void* stream);
+
+/* Profiling hook: when both events are non-NULL, the next decode call on this
+ * host thread records `before` on its stream just before the attention
+ * kernel and `after` just after it (planner and merge excluded), then clears
+ * the hook.  The events are cudaEvent_t handles passed as void*.  Used to time
+ * the attention kernel alone; it changes nothing else. */
+int mla_profile_next_decode(void* before, void* after);
+
+/* Static string naming a status code. */
+const char* mla_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,185 @@
+// C ABI of the MLA decode library: argument validation, workspace sizing,
+// tensor-map creation and the launch sequence (planner -> paired decode
+// kernel -> split merge), all on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "decode.cuh"
+
+namespace {
+
+using namespace mla;
+
+thread_local cudaEvent_t g_prof_before = nullptr, g_prof_after = nullptr;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// The bf16 cache viewed as a 2-D tensor [num_pages*64 rows, 576 columns],
+// boxes of 64 columns x 64 rows with 128-byte swizzle (one page, one chunk).
+int make_cache_tmap(CUtensorMap* m, const void* cache, int num_pages) {
+  auto fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(num_pages) * kPage};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRow) * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int validate_common(const void* q_absorbed, const void* q_rope, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, int batch, int sq, int num_heads, int num_pages, int page_size,
+                    int max_pages, float scale, const void* out, const float* lse, const void* workspace) {
+  if (!q_absorbed || !q_rope || !kv_cache || !block_table || !seq_lens || !out || !lse || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || sq <= 0 || num_pages <= 0 || max_pages <= 0 || !std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  if (num_heads != kHeads || page_size != kPage || sq > kMaxSq) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(batch) * sq > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_pages) * kPage >= INT_MAX / 2 ||
+      static_cast<long long>(max_pages) * kPage >= INT_MAX / 2)
+    return MLA_ERR_UNSUPPORTED;
+  if (!aligned(q_absorbed, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache,
+               const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads, int num_pages,
+               int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse, void* workspace,
+               size_t workspace_bytes, void* stream_ptr) {
+  int st = validate_common(q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+                           page_size, max_pages, softmax_scale, out, lse, workspace);
+  if (st != MLA_OK) return st;
+  if (fp8) return MLA_ERR_UNSUPPORTED;
+  if (batch == 0) return MLA_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int pairs = decode_max_pairs();
+  if (pairs <= 0) return MLA_ERR_CUDA;
+  const int ppg = pairs / sq > 0 ? pairs / sq : 1;
+  const WsLayout L = ws_layout(batch, sq, pairs);
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+
+  CUtensorMap tmap;
+  st = make_cache_tmap(&tmap, kv_cache, num_pages);
+  if (st != MLA_OK) return st;
+
+  if (launch_plan(seq_lens, batch, sq, max_pages, ppg, workspace, L, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  DecodeParams p;
+  p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
+  p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
+  p.kv_fp8 = nullptr;
+  p.block_table = block_table;
+  p.batch = batch;
+  p.sq = sq;
+  p.num_pages = num_pages;
+  p.max_pages = max_pages;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.ws = static_cast<uint8_t*>(workspace);
+  p.L = L;
+  cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
+  g_prof_before = g_prof_after = nullptr;
+  if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode_bf16(tmap, p, ppg * sq, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_workspace_size(int batch, int sq, int num_heads, int page_size, size_t* bytes) {
+  if (!bytes || batch < 0 || sq <= 0) return MLA_ERR_INVALID_ARG;
+  if (num_heads != kHeads || page_size != kPage || sq > kMaxSq) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(batch) * sq > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  const int pairs = decode_max_pairs();
+  if (pairs <= 0) return MLA_ERR_CUDA;
+  *bytes = ws_layout(batch > 0 ? batch : 1, sq, pairs).total;
+  return MLA_OK;
+}
+
+int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint16_t* kv_cache,
+                    const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
+                    int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return run_decode(false, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+                    page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint8_t* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
+                   int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  return run_decode(true, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+                    page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_combine_splits(const float* partial_out, const float* partial_lse, const int32_t* split_indptr, int rows,
+                       int num_heads, uint16_t* out, float* lse, void* stream) {
+  if (rows < 0 || !split_indptr || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (num_heads != kHeads) return MLA_ERR_UNSUPPORTED;
+  if (rows == 0) return MLA_OK;
+  if (!partial_out || !partial_lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned(partial_out, 16) || !aligned(out, 8)) return MLA_ERR_INVALID_ARG;
+  if (launch_combine_indptr(partial_out, partial_lse, split_indptr, rows, reinterpret_cast<__nv_bfloat16*>(out), lse,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_profile_next_decode(void* before, void* after) {
+  if ((before == nullptr) != (after == nullptr)) return MLA_ERR_INVALID_ARG;
+  g_prof_before = static_cast<cudaEvent_t>(before);
+  g_prof_after = static_cast<cudaEvent_t>(after);
+  return MLA_OK;
+}
+
+int mla_get_status(void* workspace, void* stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (v != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+  return v;
+}
+
+const char* mla_status_string(int code) {
+  switch (code) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_STATUS_BAD_PAGE: return "MLA_STATUS_BAD_PAGE";
+    case MLA_STATUS_TIMEOUT: return "MLA_STATUS_TIMEOUT";
+    case MLA_STATUS_BAD_SEQ_LEN: return "MLA_STATUS_BAD_SEQ_LEN";
+    default: return "MLA_UNKNOWN_STATUS";
+  }
+}
+
+}  // extern "C"

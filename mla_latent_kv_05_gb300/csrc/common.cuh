@@ -1,0 +1,107 @@
+// Shared constants, the workspace layout of the split-KV plan, and bounded
+// waits for the MLA decode kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mla_decode.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+constexpr int kHeads = 128;
+constexpr int kDc = 512;            // latent c_KV
+constexpr int kDr = 64;             // decoupled RoPE key
+constexpr int kRow = kDc + kDr;     // 576 values per cached token
+constexpr int kPage = 64;           // tokens per page (= tokens per KV tile)
+constexpr int kFp8Row = kRow + kRow / 32;   // 594 bytes
+constexpr int kMaxSq = 4;
+constexpr int kMaxRows = 1 << 16;   // batch * Sq handled by the planner
+
+// Plan header at workspace offset 0.
+struct PlanHeader {
+  int status;            // first device-side problem seen (0 = none)
+  int n_tiles;           // total KV tiles over the batch (longest query)
+  int chunk;             // tiles per pair
+  int slots_per_query;   // partial slots of one query index
+  int n_comb;            // rows the merge kernel must write
+  int pairs_per_group;   // pairs that serve one query index
+  int abort_flag;        // set by the first wait that times out; all waits then give up
+  int pad[9];
+};
+
+// Offsets (bytes) of the plan arrays and split partials inside the workspace.
+struct WsLayout {
+  size_t lens, tile_start, first_pair, slot_base, comb_row, comb_start, comb_count;
+  size_t part_lse, part_out, total;
+  int max_slots;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+__host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs) {
+  WsLayout L;
+  const int pg = pairs / sq > 0 ? pairs / sq : 1;
+  // every pair boundary splits at most one row: slots per query <= 2*(pg-1)
+  L.max_slots = sq * 2 * pg;
+  size_t o = align256(sizeof(PlanHeader));
+  L.lens = o;        o = align256(o + sizeof(int) * batch);
+  L.tile_start = o;  o = align256(o + sizeof(int) * (batch + 1));
+  L.first_pair = o;  o = align256(o + sizeof(int) * batch);
+  L.slot_base = o;   o = align256(o + sizeof(int) * batch);
+  L.comb_row = o;    o = align256(o + sizeof(int) * batch * sq);
+  L.comb_start = o;  o = align256(o + sizeof(int) * batch * sq);
+  L.comb_count = o;  o = align256(o + sizeof(int) * batch * sq);
+  L.part_lse = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads);
+  L.part_out = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads * kDc);
+  L.total = o;
+  return L;
+}
+
+// Record the first problem seen (never overwrites an earlier one).
+__device__ __forceinline__ void set_status(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ int read_status(const int* status) {
+  return *reinterpret_cast<const volatile int*>(status);
+}
+
+#ifndef MLA_WAIT_TIMEOUT_NS
+#define MLA_WAIT_TIMEOUT_NS 2000000000ull   // 2 s: far beyond any legal wait
+#endif
+
+// Bounded mbarrier wait.  Returns false (after recording MLA_STATUS_TIMEOUT)
+// if the phase did not complete within the time limit, or if another thread
+// of the grid already gave up; the caller then leaves its loop.
+// `hdr` is the plan header in global memory.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, PlanHeader* hdr) {
+  auto poll = [&]() {
+    return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (poll()) return true;
+    if ((n & 255u) == 0) {
+      if (read_status(&hdr->abort_flag) != 0) return false;
+      if (ptx::globaltimer() - t0 > MLA_WAIT_TIMEOUT_NS) {
+        set_status(&hdr->status, MLA_STATUS_TIMEOUT);
+        atomicExch(&hdr->abort_flag, 1);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: every lane polls (so every lane acquires the
+// phase), and the warp leaves together if any lane gave up.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, PlanHeader* hdr) {
+  const bool ok = wait_bounded<kCluster>(bar, parity, hdr);
+  return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace mla

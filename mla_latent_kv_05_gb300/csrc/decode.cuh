@@ -1,0 +1,32 @@
+// Parameters and host launchers of the MLA decode kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace mla {
+
+struct DecodeParams {
+  const __nv_bfloat16* q_abs;    // [B, Sq, 128, 512]
+  const __nv_bfloat16* q_rope;   // [B, Sq, 128, 64]
+  const uint8_t* kv_fp8;         // fp8 cache [P, 64, 594] (fp8 mode)
+  const int32_t* block_table;    // [B, max_pages]
+  int batch, sq, num_pages, max_pages;
+  float scale_log2;              // softmax scale * log2(e)
+  __nv_bfloat16* out;            // [B, Sq, 128, 512]
+  float* lse;                    // [B, Sq, 128]
+  uint8_t* ws;
+  WsLayout L;
+};
+
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_pages, int pairs_per_group,
+                        void* ws, const WsLayout& L, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const CUtensorMap& tmap, const DecodeParams& p, int n_pairs, cudaStream_t stream);
+int decode_max_pairs();
+cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows, __nv_bfloat16* out, float* lse,
+                                cudaStream_t stream);
+cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,
+                                  __nv_bfloat16* out, float* lse, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,61 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point
+include/mla_decode.h declares, and rejects bad arguments on the host before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_latent_kv_05_gb300 import _build, binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("mla_decode_bf16", "mla_decode_fp8", "mla_combine_splits", "mla_workspace_size",
+              "mla_get_status", "mla_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(binding.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in binding._STATUS.items():
+        assert lib.mla_status_string(code).decode() == name
+
+
+def test_host_validation_without_gpu(lib):
+    z = ctypes.c_void_p(0)
+    rc = lib.mla_decode_bf16(z, z, z, z, z, 1, 1, 128, 8, 64, 4, ctypes.c_float(0.1), z, z, z, 0, z)
+    assert rc == -1
+    n = ctypes.c_size_t(0)
+    assert lib.mla_workspace_size(1, 1, 64, 64, ctypes.byref(n)) == -2     # num_heads != 128
+    assert lib.mla_workspace_size(1, 1, 128, 32, ctypes.byref(n)) == -2    # page_size != 64
+    assert lib.mla_workspace_size(1, 5, 128, 64, ctypes.byref(n)) == -2    # Sq > 4
+    assert lib.mla_workspace_size(1, 0, 128, 64, ctypes.byref(n)) == -1
+    assert lib.mla_combine_splits(z, z, z, -1, 128, z, z, z) == -1
+    fake = ctypes.c_void_p(0x1000)
+    rc = lib.mla_decode_bf16(fake, fake, fake, fake, fake, 1, 1, 64, 8, 64, 4, ctypes.c_float(0.1),
+                             fake, fake, fake, 1 << 30, z)
+    assert rc == -2
+    rc = lib.mla_decode_fp8(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(float("nan")),
+                            fake, fake, fake, 1 << 30, z)
+    assert rc == -1

@@ -1,0 +1,188 @@
+"""GPU parity of the CUDA decode path (through the C ABI) against the float64
+oracle, on small seeded problems that span several tiles, ragged tails,
+split-KV, multi-token causal queries and the degenerate cases.
+
+Bounds: max|out - ref| <= 1e-2 * max|ref| and max|lse - ref| <= 1e-3;
+bit-exact where the result is a copy (one visible token).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mla_latent_kv_05_gb300 import binding
+from mla_latent_kv_05_gb300 import inputs as gen
+from oracle import mla_oracle
+
+pytestmark = pytest.mark.gpu
+
+OUT_RTOL = 1e-2
+LSE_ATOL = 1e-3
+
+
+def to_dev(inp, dev="cuda"):
+    return dict(q=inp.q_absorbed.to(dev), qr=inp.q_rope.to(dev), kv=inp.kv_cache.to(dev),
+                bt=inp.block_table.to(dev), sl=inp.seq_lens.to(dev))
+
+
+def run_gpu(inp, d=None):
+    d = d or to_dev(inp)
+    ws = binding.alloc_workspace(inp.batch, inp.sq)
+    fn = binding.mla_decode_bf16 if inp.kv_dtype == "bf16" else binding.mla_decode_fp8
+    out, lse = fn(d["q"], d["qr"], d["kv"], d["bt"], d["sl"], inp.scale, workspace=ws)
+    st = binding.mla_get_status(ws)
+    return out, lse, st
+
+
+def oracle(inp, query_rows=None):
+    raw = inp.kv_cache.double().numpy() if inp.kv_dtype == "bf16" else inp.kv_cache.numpy()
+    rows = mla_oracle.cache_rows(raw, inp.kv_dtype)
+    return mla_oracle.mla_decode(inp.q_absorbed.double().numpy(), inp.q_rope.double().numpy(), rows,
+                                 inp.block_table.numpy(), inp.seq_lens.numpy(), inp.scale, query_rows)
+
+
+def assert_close(out, lse, ref_out, ref_lse, query_rows=None):
+    got = out.double().cpu().numpy()
+    gl = lse.double().cpu().numpy()
+    if query_rows is None:
+        query_rows = [(b, i) for b in range(got.shape[0]) for i in range(got.shape[1])]
+    for b, i in query_rows:
+        r, rl = ref_out[b, i], ref_lse[b, i]
+        if np.all(np.isneginf(rl)):
+            assert np.all(got[b, i] == 0), (b, i)
+            assert np.all(np.isneginf(gl[b, i])), (b, i)
+            continue
+        err = np.abs(got[b, i] - r).max()
+        bound = OUT_RTOL * np.abs(r).max()
+        assert err <= bound, f"row ({b},{i}): max|dout| {err:.3e} > {bound:.3e}"
+        lerr = np.abs(gl[b, i] - rl).max()
+        assert lerr <= LSE_ATOL, f"row ({b},{i}): max|dlse| {lerr:.3e}"
+
+
+def test_workload1_oracle_sized(cuda_device):
+    inp = gen.make_workload(1)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+@pytest.mark.parametrize("lens", [
+    [1, 2, 63, 64, 65, 127, 128, 129],
+    [1000, 4097, 3, 700],
+    [5000],
+])
+def test_ragged_lengths(cuda_device, lens):
+    inp = gen.make_inputs(len(lens), 1, lens, seed=sum(lens))
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+@pytest.mark.parametrize("sq,lens", [(2, [1, 2, 64, 65, 300]), (2, [129, 4096]), (3, [3, 64, 200]), (4, [70])])
+def test_multi_token_causal(cuda_device, sq, lens):
+    inp = gen.make_inputs(len(lens), sq, lens, seed=17 + sq)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_empty_rows(cuda_device):
+    inp = gen.make_inputs(4, 1, [0, 70, 0, 1], seed=3, physical_pages=4)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_single_token_is_bit_exact_copy(cuda_device):
+    lens = [1] * 6
+    inp = gen.make_inputs(6, 1, lens, seed=21)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(6):
+        page = int(inp.block_table[b, 0])
+        row = inp.kv_cache[page, 0, :512]
+        assert torch.equal(out[b, 0].cpu(), row.expand(128, 512)), b
+    ref_out, ref_lse = oracle(inp)
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= LSE_ATOL
+
+
+def test_unused_slots_hold_nan(cuda_device):
+    lens = [70, 130, 1]
+    inp = gen.make_inputs(3, 1, lens, seed=5)
+    ref = oracle(inp)
+    for b, s in enumerate(lens):
+        page = int(inp.block_table[b, (s - 1) // 64])
+        inp.kv_cache[page, s % 64 if s % 64 else 64:, :] = float("nan")
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, lse, *ref)
+
+
+def test_page_permutation_gives_identical_bits(cuda_device):
+    lens = [300, 77]
+    inp = gen.make_inputs(2, 1, lens, seed=9, physical_pages=12)
+    out1, lse1, _ = run_gpu(inp)
+    perm = torch.randperm(inp.num_pages, generator=torch.Generator().manual_seed(1))
+    inv = torch.argsort(perm)
+    kv2 = inp.kv_cache[perm].contiguous()
+    bt2 = torch.where(inp.block_table >= 0, inv[inp.block_table.clamp(min=0).long()].int(), inp.block_table)
+    inp2 = gen.DecodeInputs(inp.q_absorbed, inp.q_rope, kv2, bt2, inp.seq_lens, inp.scale, "bf16")
+    out2, lse2, _ = run_gpu(inp2)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_growing_scores_exercise_rescale(cuda_device):
+    """Scores that rise along the sequence make the reference max move by
+    more than the lazy-rescale threshold many times."""
+    n = 2000
+    inp = gen.make_inputs(1, 1, [n], seed=2)
+    pages = inp.block_table[0, : (n + 63) // 64]
+    for j in range(n):
+        inp.kv_cache[pages[j // 64], j % 64, 0] = j * 0.02
+    inp.q_absorbed[..., 0] = torch.linspace(1, 60, 128).to(torch.bfloat16)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_bad_page_and_bad_length_set_status(cuda_device):
+    inp = gen.make_inputs(2, 1, [100, 64], seed=4)
+    inp.block_table[0, 1] = inp.num_pages + 7
+    _, _, st = run_gpu(inp)
+    assert st == -5
+    inp = gen.make_inputs(2, 1, [100, 64], seed=4)
+    inp.seq_lens[1] = inp.max_pages * 64 + 1
+    _, _, st = run_gpu(inp)
+    assert st == -7
+
+
+def test_workspace_too_small_is_rejected(cuda_device):
+    inp = gen.make_inputs(1, 1, [64], seed=4)
+    d = to_dev(inp)
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.MLAError) as e:
+        binding.mla_decode_bf16(d["q"], d["qr"], d["kv"], d["bt"], d["sl"], inp.scale, workspace=ws)
+    assert e.value.code == -3
+
+
+def test_combine_splits_matches_oracle_merge(cuda_device):
+    rng = np.random.default_rng(0)
+    counts = [1, 3, 0, 2]
+    n = sum(counts)
+    po = rng.standard_normal((n, 128, 512)).astype(np.float32)
+    pl = (rng.standard_normal((n, 128)) * 3).astype(np.float32)
+    pl[1, :5] = -np.inf
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    out, lse = binding.mla_combine_splits(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(),
+                                          torch.from_numpy(indptr).cuda())
+    torch.cuda.synchronize()
+    for r in range(len(counts)):
+        a, b = indptr[r], indptr[r + 1]
+        ro, rl = mla_oracle.merge_partials(po[a:b].astype(np.float64), pl[a:b].astype(np.float64))
+        if b == a:
+            assert torch.all(out[r] == 0) and torch.all(torch.isneginf(lse[r]))
+            continue
+        np.testing.assert_allclose(out[r].double().cpu().numpy(), ro, atol=1e-2 * np.abs(ro).max())
+        np.testing.assert_allclose(lse[r].double().cpu().numpy(), rl, atol=1e-5)
