@@ -1,8 +1,7 @@
 // Split-KV merge.  Attention over disjoint token sets combines exactly from
 // each part's normalised output and LSE:
 //     L = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - L) * out_s.
-// One CTA per output row, one warp per group of heads, 16 fp32 per lane
-// (float4 loads), bf16 out.
+// One warp per (output row, head), 16 fp32 per lane (float4 loads), bf16 out.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -11,7 +10,8 @@ namespace mla {
 
 namespace {
 
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_out,
+// grid (rows, 128 / 8): one warp per (row, head); 16 fp32 per lane.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
                                                       const float* __restrict__ part_lse,
                                                       const int32_t* __restrict__ row_start,
                                                       const int32_t* __restrict__ row_count,
@@ -25,43 +25,44 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   const int count = row_count ? row_count[k] : row_start[k + 1] - start;   // null: row_start is an indptr
   const int row = row_index ? row_index[k] : k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int h = warp; h < kHeads; h += 4) {
-    float L = -INFINITY;
+  const int h = blockIdx.y * 8 + warp;
+  // each lane reads one part's lse (parts beyond 32 loop), then a warp max / sum
+  float L = -INFINITY;
+  for (int s = lane; s < count; s += 32) L = fmaxf(L, part_lse[static_cast<size_t>(start + s) * kHeads + h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  float sum = 0.f;
+  if (L != -INFINITY) {
     for (int s = 0; s < count; ++s) {
       const float v = part_lse[static_cast<size_t>(start + s) * kHeads + h];
-      if (v > L) L = v;
-    }
-    float acc[16];
+      const float wgt = v == -INFINITY ? 0.f : __expf(v - L);
+      sum += wgt;
+      const float4* src = reinterpret_cast<const float4*>(part_out + (static_cast<size_t>(start + s) * kHeads + h) * kDc);
+      float4 x[4];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-    float sum = 0.f;
-    if (L != -INFINITY) {
-      for (int s = 0; s < count; ++s) {
-        const float v = part_lse[static_cast<size_t>(start + s) * kHeads + h];
-        const float wgt = v == -INFINITY ? 0.f : __expf(v - L);
-        sum += wgt;
-        const float4* src = reinterpret_cast<const float4*>(part_out + (static_cast<size_t>(start + s) * kHeads + h) * kDc);
+      for (int q = 0; q < 4; ++q) x[q] = __ldcs(src + q * 32 + lane);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 x = src[q * 32 + lane];
-          acc[4 * q] += wgt * x.x; acc[4 * q + 1] += wgt * x.y;
-          acc[4 * q + 2] += wgt * x.z; acc[4 * q + 3] += wgt * x.w;
-        }
+      for (int q = 0; q < 4; ++q) {
+        acc[4 * q] += wgt * x[q].x; acc[4 * q + 1] += wgt * x[q].y;
+        acc[4 * q + 2] += wgt * x[q].z; acc[4 * q + 3] += wgt * x[q].w;
       }
     }
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    __nv_bfloat16* dst = out + (static_cast<size_t>(row) * kHeads + h) * kDc;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * q] * inv, acc[4 * q + 1] * inv);
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv);
-      uint2 v;
-      v.x = *reinterpret_cast<uint32_t*>(&a);
-      v.y = *reinterpret_cast<uint32_t*>(&b);
-      reinterpret_cast<uint2*>(dst)[q * 32 + lane] = v;
-    }
-    if (lane == 0) lse[static_cast<size_t>(row) * kHeads + h] = sum > 0.f ? L + logf(sum) : -INFINITY;
   }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  __nv_bfloat16* dst = out + (static_cast<size_t>(row) * kHeads + h) * kDc;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * q] * inv, acc[4 * q + 1] * inv);
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&a);
+    v.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(dst)[q * 32 + lane] = v;
+  }
+  if (lane == 0) lse[static_cast<size_t>(row) * kHeads + h] = sum > 0.f ? L + logf(sum) : -INFINITY;
 }
 
 }  // namespace
@@ -71,7 +72,7 @@ cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows
                                 cudaStream_t stream) {
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   if (max_rows <= 0) return cudaSuccess;
-  combine_kernel<<<max_rows, 128, 0, stream>>>(
+  combine_kernel<<<dim3(max_rows, kHeads / 8), 256, 0, stream>>>(
       reinterpret_cast<const float*>(w + Lw.part_out), reinterpret_cast<const float*>(w + Lw.part_lse),
       reinterpret_cast<const int32_t*>(w + Lw.comb_start), reinterpret_cast<const int32_t*>(w + Lw.comb_count),
       reinterpret_cast<const int32_t*>(w + Lw.comb_row),
@@ -83,7 +84,7 @@ cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows
 cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,
                                   __nv_bfloat16* out, float* lse, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  combine_kernel<<<rows, 128, 0, stream>>>(part_out, part_lse, indptr, nullptr, nullptr, nullptr, rows, out, lse);
+  combine_kernel<<<dim3(rows, kHeads / 8), 256, 0, stream>>>(part_out, part_lse, indptr, nullptr, nullptr, nullptr, rows, out, lse);
   return cudaGetLastError();
 }
 

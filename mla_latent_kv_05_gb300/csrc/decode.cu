@@ -115,10 +115,8 @@ struct SegWalker {
   }
 };
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi, float& lo_r, float& hi_r) {
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  lo_r = __low2float(v);
-  hi_r = __high2float(v);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -329,15 +327,23 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
         const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<size_t>(row) * kHeads + h) * kDc);
         const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + (static_cast<size_t>(row) * kHeads + h) * kDr);
 #pragma unroll 1
-        for (int cc = 0; cc < 9; ++cc) {
-          uint32_t r[32];
-          const uint4* src = cc < 8 ? qa + cc * 8 : qr;
+        for (int c3 = 0; c3 < 3; ++c3) {          // three chunks of 32 columns per round trip
+          uint4 x[24];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 x = __ldg(src + v);
-            r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+          for (int v = 0; v < 24; ++v) {
+            const int cc = c3 * 3 + v / 8;
+            x[v] = __ldg((cc < 8 ? qa + cc * 8 : qr) + (v & 7));
           }
-          ptx::tmem_st32(tmem + lane_base + kQCol + 32u * cc, r);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            uint32_t r[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              r[4 * v] = x[8 * j + v].x; r[4 * v + 1] = x[8 * j + v].y;
+              r[4 * v + 2] = x[8 * j + v].z; r[4 * v + 3] = x[8 * j + v].w;
+            }
+            ptx::tmem_st32(tmem + lane_base + kQCol + 32u * (c3 * 3 + j), r);
+          }
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -375,9 +381,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
           const float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
           const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - m_ref);
           const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - m_ref);
-          float r0, r1;
-          pk[e] = pack_bf16x2(p0, p1, r0, r1);
-          l += r0 + r1;
+          pk[e] = pack_bf16x2(p0, p1);
+          l += p0 + p1;
         }
         if (!wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr)) { ok = false; break; }
         const uint32_t prow = ptx::mapa(sbase + kOffAux + static_cast<uint32_t>(ps) * kPSlotBytes + h * 128u, 0);
