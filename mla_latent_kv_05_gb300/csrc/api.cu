@@ -71,7 +71,6 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   int st = validate_common(q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
                            page_size, max_pages, softmax_scale, out, lse, workspace);
   if (st != MLA_OK) return st;
-  if (fp8) return MLA_ERR_UNSUPPORTED;
   if (batch == 0) return MLA_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int pairs = decode_max_pairs();
@@ -81,14 +80,16 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
   CUtensorMap tmap;
-  st = make_cache_tmap(&tmap, kv_cache, num_pages);
-  if (st != MLA_OK) return st;
+  if (!fp8) {
+    st = make_cache_tmap(&tmap, kv_cache, num_pages);
+    if (st != MLA_OK) return st;
+  }
 
   if (launch_plan(seq_lens, batch, sq, max_pages, ppg, workspace, L, stream) != cudaSuccess) return MLA_ERR_CUDA;
   DecodeParams p;
   p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
   p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
-  p.kv_fp8 = nullptr;
+  p.kv_fp8 = fp8 ? static_cast<const uint8_t*>(kv_cache) : nullptr;
   p.block_table = block_table;
   p.batch = batch;
   p.sq = sq;
@@ -102,7 +103,8 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
   g_prof_before = g_prof_after = nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_decode_bf16(tmap, p, ppg * sq, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t le = fp8 ? launch_decode_fp8(p, ppg * sq, stream) : launch_decode_bf16(tmap, p, ppg * sq, stream);
+  if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;

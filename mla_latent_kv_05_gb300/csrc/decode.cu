@@ -13,8 +13,9 @@
 //       S = Q . K^T with A read from TMEM (kind::f16, M=128, N=64, K=576),
 //       double-buffered S in TMEM, online softmax in 4 warps (thread = head
 //       row, so row max / row sum need no cross-thread reduction), P rounded
-//       to bf16 and stored straight into rank 0's shared memory in the
-//       128B-swizzled K-major layout the MMA reads;
+//       to bf16 and sent with st.async straight into rank 0's shared memory
+//       in the 128B-swizzled K-major layout the MMA reads (the bytes are
+//       counted on rank 0's barrier, so no thread waits for the transfer);
 //   rank 0 ("value SM"):  O [128 x 512] fp32 in all of its TMEM,
 //       O += P . V with P from shared memory (K-major) and V read from the
 //       page tile as an MN-major operand (two M=128, N=256, K=16 MMAs per
@@ -35,6 +36,9 @@
 // abort flag so all waits of the grid give up and the kernel exits cleanly.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
 
 #include "decode.cuh"
 
@@ -44,26 +48,55 @@ namespace dk {
 
 constexpr uint32_t kChunkBytes = 64 * 128;            // 64 rows x 64 bf16, 128B swizzle
 constexpr uint32_t kStageBytes = 8 * kChunkBytes;     // latent c_KV part of one page
-constexpr int kStages = 3;
-constexpr uint32_t kOffAux = kStages * kStageBytes;   // rank 1: RoPE ring; rank 0: P ring
 constexpr uint32_t kPSlotBytes = 128 * 128;           // P tile: 128 heads x 64 tokens bf16
 constexpr int kPSlots = 2;
-constexpr uint32_t kOffAlpha = kOffAux + kPSlots * kPSlotBytes;  // rank 0: fp32 [2][128]
 constexpr int kMailSlots = 2;
-constexpr uint32_t kOffMail = kOffAlpha + kPSlots * 128 * 4;     // rank 0: 1/l [2][128]
-constexpr uint32_t kOffFlag = kOffMail + kMailSlots * 128 * 4;   // rank 0: slot of a rescale request
-constexpr uint32_t kOffBar = kOffFlag + 16;
+constexpr uint32_t kRawBytes = 32 * kFp8Row;          // half a page of FP8 rows: 19,008 B
+constexpr int kMaxRaw = 4;
+
+// Shared-memory plans.  The operand ring holds bf16 page tiles in the
+// 128B-swizzled layout the MMAs read (latent chunks at stage*64K + c*8K);
+// behind it rank 1 keeps the RoPE chunk of each stage and rank 0 its P slots.
+// The FP8 plan adds a ring of raw half pages per rank.  Both ranks put the
+// small shared region (alpha, 1/l, flags, barriers) at the same offset so
+// remote stores and arrivals can address it by offset.
+template <int kMode> struct Cfg;
+template <> struct Cfg<0> {            // bf16 cache: 2-D TMA tiles
+  static constexpr int kStages = 3;
+  static constexpr int kRawStages1 = 0, kRawStages0 = 0;
+  static constexpr uint32_t kOffAux = kStages * kStageBytes;
+  static constexpr uint32_t kOffRaw1 = 0, kOffRaw0 = 0;
+  static constexpr uint32_t kOffMisc = kOffAux + kPSlots * kPSlotBytes;
+  static constexpr int kThreads = 256;
+};
+template <> struct Cfg<1> {            // FP8 cache: 1-D bulk copies + dequant warps 8..11
+  static constexpr int kStages = 2;
+  static constexpr int kRawStages1 = 4, kRawStages0 = 3;
+  static constexpr uint32_t kOffAux = kStages * kStageBytes;
+  static constexpr uint32_t kOffRaw1 = kOffAux + kStages * kChunkBytes;   // after the RoPE ring
+  static constexpr uint32_t kOffRaw0 = kOffAux + kPSlots * kPSlotBytes;   // after the P ring
+  static constexpr uint32_t kOffMisc = kOffRaw1 + kRawStages1 * kRawBytes;
+  static constexpr int kThreads = 384;
+};
+constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
+constexpr uint32_t kMiscMail = 1024;     // rank 0: fp32 1/l [2][128]
+constexpr uint32_t kMiscReq = 2048;      // rank 0: P slot of a rescale request
+constexpr uint32_t kMiscRawBad = 2064;   // per raw stage: 1 if its page id was out of range
+constexpr uint32_t kMiscBar = 2080;
 enum Bar {
-  FULL = 0, EMPTY = FULL + kStages,
-  PFULL = EMPTY + kStages, PEMPTY = PFULL + kPSlots,
+  FULL = 0, EMPTY = FULL + 3,
+  PFULL = EMPTY + 3, PEMPTY = PFULL + kPSlots,
   SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + 2,
   QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
-  NBAR = MBEMPTY + kMailSlots
+  RAWFULL = MBEMPTY + kMailSlots, RAWEMPTY = RAWFULL + kMaxRaw,
+  NBAR = RAWEMPTY + kMaxRaw
 };
-constexpr uint32_t kOffTmemPtr = kOffBar + NBAR * 8;
-constexpr uint32_t kSmemBytes = kOffTmemPtr + 16;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kMiscTmem = kMiscBar + NBAR * 8;
+constexpr uint32_t kMiscBytes = kMiscTmem + 16;
+template <int kMode> constexpr uint32_t smem_bytes() { return Cfg<kMode>::kOffMisc + kMiscBytes; }
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory budget");
+static_assert(Cfg<1>::kOffRaw0 + Cfg<1>::kRawStages0 * kRawBytes <= Cfg<1>::kOffMisc, "rank 0 raw ring");
 
 // TMEM columns.
 constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
@@ -120,12 +153,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 32 e4m3 codes (8 words, lowest byte first) with their e8m0 scale byte ->
+// 16 bf16x2 words.  e4m3 -> f16 is exact in hardware, the product with the
+// power-of-two scale is exact in fp32 (no flush), and the result has at most
+// 4 significant bits, so the bf16 rounding is exact too.  NaN codes and the
+// NaN scale (0xFF) give NaN, as in the format definitions.
+__device__ __forceinline__ void dequant32(const uint32_t* wd, uint32_t e, uint32_t* o) {
+  const float sc = __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : (e << 23)));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t h01, h23;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<unsigned short>(wd[i] & 0xFFFFu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<unsigned short>(wd[i] >> 16)));
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    o[2 * i] = pack_bf16x2(f01.x * sc, f01.y * sc);
+    o[2 * i + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
+  }
+}
+
 }  // namespace dk
 
-template <int kMode>   // 0: bf16 cache via TMA
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+template <int kMode>   // 0: bf16 cache via TMA, 1: FP8 cache via bulk copies + dequant
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dk::Cfg<kMode>::kThreads, 1)
 mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   using namespace dk;
+  using C = Cfg<kMode>;
+  constexpr int kStages = C::kStages;
+  constexpr uint32_t kOffAux = C::kOffAux;
+  constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
+  constexpr uint32_t kOffMail = C::kOffMisc + kMiscMail;
+  constexpr uint32_t kOffFlag = C::kOffMisc + kMiscReq;
+  constexpr uint32_t kOffRawBad = C::kOffMisc + kMiscRawBad;
+  constexpr uint32_t kOffBar = C::kOffMisc + kMiscBar;
+  constexpr uint32_t kOffTmemPtr = C::kOffMisc + kMiscTmem;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t rank = ptx::cluster_ctarank();
@@ -143,7 +204,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
   const bool smem_ok = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
     if (!smem_ok) set_status(&hdr->status, MLA_ERR_UNSUPPORTED);
-    for (int s = 0; s < kStages; ++s) { ptx::mbar_init(BAR(FULL + s), 1); ptx::mbar_init(BAR(EMPTY + s), 1); }
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(BAR(FULL + s), kMode == 0 ? 1 : 4);   // TMA bytes, or the 4 dequant warps
+      ptx::mbar_init(BAR(EMPTY + s), 1);
+    }
+    for (int s = 0; s < kMaxRaw; ++s) { ptx::mbar_init(BAR(RAWFULL + s), 1); ptx::mbar_init(BAR(RAWEMPTY + s), 4); }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128); ptx::mbar_init(BAR(PEMPTY + s), 1); }
     for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128); }
     ptx::mbar_init(BAR(QREADY), 128);
@@ -176,32 +241,122 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
   const bool active = smem_ok && group < sq;
 
   if (active && warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = ptx::policy_evict_first();
+      const uint64_t pol = ptx::policy_evict_normal();
       SegWalker w; w.init(tile_start, p.batch, lo, hi);
       Segment sg;
       int stage = 0; uint32_t phase = 0;
+      int rs = 0; uint32_t rphase = 0;
+      const int n_raw = rank == 1 ? C::kRawStages1 : C::kRawStages0;
+      const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
+      volatile uint32_t* raw_bad = reinterpret_cast<volatile uint32_t*>(smem + kOffRawBad);
       bool ok = true;
       while (ok && w.next(sg)) {
         for (int t = sg.t0; t < sg.t1; ++t) {
           int page = __ldg(p.block_table + static_cast<size_t>(sg.b) * p.max_pages + t);
-          if (page < 0 || page >= p.num_pages) {
-            set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
-            page = p.num_pages;          // fully out of the tensor: TMA fills zeros
-          }
-          if (!wait_bounded<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
-          const uint32_t bytes = (rank == 1 ? 9u : 8u) * kChunkBytes;
-          ptx::mbar_arrive_expect_tx(BAR(FULL + stage), bytes);
-          const int y = page * kPage;
-          const uint32_t dst = sbase + static_cast<uint32_t>(stage) * kStageBytes;
+          const bool bad = page < 0 || page >= p.num_pages;
+          if (bad) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
+          if constexpr (kMode == 0) {
+            if (bad) page = p.num_pages;   // fully outside the tensor: TMA fills zeros
+            if (!wait_bounded<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
+            const uint32_t bytes = (rank == 1 ? 9u : 8u) * kChunkBytes;
+            ptx::mbar_arrive_expect_tx(BAR(FULL + stage), bytes);
+            const int y = page * kPage;
+            const uint32_t dst = sbase + static_cast<uint32_t>(stage) * kStageBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            ptx::tma_load_2d(dst + c * kChunkBytes, &tmap, BAR(FULL + stage), c * 64, y, pol);
-          if (rank == 1)
-            ptx::tma_load_2d(sbase + kOffAux + stage * kChunkBytes, &tmap, BAR(FULL + stage), 512, y, pol);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            for (int c = 0; c < 8; ++c)
+              ptx::tma_load_2d(dst + c * kChunkBytes, &tmap, BAR(FULL + stage), c * 64, y, pol);
+            if (rank == 1)
+              ptx::tma_load_2d(sbase + kOffAux + stage * kChunkBytes, &tmap, BAR(FULL + stage), 512, y, pol);
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          } else {
+            // two half pages of raw FP8 rows; a bad page is never read (zeros)
+            for (int half = 0; half < 2; ++half) {
+              if (!wait_bounded<true>(BAR(RAWEMPTY + rs), rphase ^ 1u, hdr)) { ok = false; break; }
+              raw_bad[rs] = bad ? 1u : 0u;
+              if (bad) {
+                ptx::mbar_arrive(BAR(RAWFULL + rs));
+              } else {
+                ptx::mbar_arrive_expect_tx(BAR(RAWFULL + rs), kRawBytes);
+                const uint8_t* src = p.kv_fp8 + static_cast<size_t>(page) * (kPage * kFp8Row) + half * kRawBytes;
+                ptx::bulk_load(sbase + raw_off + static_cast<uint32_t>(rs) * kRawBytes, src, kRawBytes,
+                               BAR(RAWFULL + rs), pol);
+              }
+              if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
+            }
+            if (!ok) break;
+          }
         }
+      }
+    }
+  } else if (kMode == 1 && active && warp >= 8) {
+    // ------------------------------------------------------------ FP8 dequant (warps 8..11)
+    // raw half page -> bf16 operand tile rows [32*half, 32*half+32).  Warp
+    // wq handles tokens of parity (wq & 1) and half of the 32-value groups
+    // (9 of 18 on rank 1, 8 of the 16 latent groups on rank 0).
+    const int wq = warp - 8;
+    const int parity = wq & 1;
+    const int G = rank == 1 ? 9 : 8;
+    const int g0 = (wq >> 1) * G;
+    const int n_tasks = 16 * G;
+    const int n_raw = rank == 1 ? C::kRawStages1 : C::kRawStages0;
+    const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
+    const volatile uint32_t* raw_bad = reinterpret_cast<const volatile uint32_t*>(smem + kOffRawBad);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    Segment sg;
+    int stage = 0; uint32_t phase = 0;
+    int rs = 0; uint32_t rphase = 0;
+    bool ok = true;
+    while (ok && w.next(sg)) {
+      for (int t = sg.t0; t < sg.t1 && ok; ++t) {
+        if (!wait_warp<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
+        for (int half = 0; half < 2; ++half) {
+          if (!wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
+          const bool bad = raw_bad[rs] != 0;
+          const uint8_t* raw = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes;
+          for (int task = lane; task < n_tasks; task += 32) {
+            const int tok = 2 * (task / G) + parity;          // token within the half page
+            const int g = g0 + task % G;                       // 32-value group
+            const int tp = 32 * half + tok;                    // row within the page tile
+            uint32_t o[16];
+            if (!bad) {
+              const uint8_t* src = raw + tok * kFp8Row + 32 * g;
+              uint32_t wd[8];
+              if (parity == 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) wd[i] = reinterpret_cast<const uint32_t*>(src)[i];
+              } else {
+                const uint32_t* a = reinterpret_cast<const uint32_t*>(src - 2);
+                uint32_t u[9];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) u[i] = a[i];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) wd[i] = __funnelshift_r(u[i], u[i + 1], 16);
+              }
+              dequant32(wd, raw[tok * kFp8Row + kRow + g], o);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = 0u;
+            }
+            const int c = g >> 1;
+            uint8_t* dst = smem + (c < 8 ? static_cast<uint32_t>(stage) * kStageBytes + c * kChunkBytes
+                                         : kOffAux + static_cast<uint32_t>(stage) * kChunkBytes) + tp * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int piece = ((g & 1) * 4 + j) ^ (tp & 7);
+              *reinterpret_cast<uint4*>(dst + piece * 16) = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
+          }
+          ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA (async proxy)
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(BAR(RAWEMPTY + rs));
+          if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(BAR(FULL + stage));
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (active && warp == 1 && rank == 1) {
@@ -385,13 +540,16 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
           l += p0 + p1;
         }
         if (!wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr)) { ok = false; break; }
+        // P row h (128 B, swizzled) and alpha_h go to rank 0 as st.async
+        // bytes counted on its PFULL barrier: nobody waits for them here.
+        const uint32_t pfull = ptx::mapa(BAR(PFULL + ps), 0);
+        ptx::mbar_arrive_expect_tx_remote(pfull, 8u * 16u + 4u);
         const uint32_t prow = ptx::mapa(sbase + kOffAux + static_cast<uint32_t>(ps) * kPSlotBytes + h * 128u, 0);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          ptx::st_cluster_v4(prow + ((j ^ (h & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        ptx::st_cluster_b32(ptx::mapa(sbase + kOffAlpha + ps * 512u + h * 4u, 0), __float_as_uint(alpha));
-        ptx::fence_proxy_async_cluster();
-        ptx::mbar_arrive_remote(ptx::mapa(BAR(PFULL + ps), 0));
+          ptx::st_async_v4(prow + ((j ^ (h & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3],
+                           pfull);
+        ptx::st_async_b32(ptx::mapa(sbase + kOffAlpha + ps * 512u + h * 4u, 0), __float_as_uint(alpha), pfull);
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
@@ -403,8 +561,9 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
       if (split) part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
       else p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
       if (!wait_warp<true>(BAR(MBEMPTY + ms), mphase ^ 1u, hdr)) { ok = false; break; }
-      ptx::st_cluster_b32(ptx::mapa(sbase + kOffMail + ms * 512u + h * 4u, 0), __float_as_uint(inv_l));
-      ptx::mbar_arrive_remote(ptx::mapa(BAR(MBFULL + ms), 0));
+      const uint32_t mbfull = ptx::mapa(BAR(MBFULL + ms), 0);
+      ptx::mbar_arrive_expect_tx_remote(mbfull, 4u);
+      ptx::st_async_b32(ptx::mapa(sbase + kOffMail + ms * 512u + h * 4u, 0), __float_as_uint(inv_l), mbfull);
       if (++ms == kMailSlots) { ms = 0; mphase ^= 1u; }
     }
     // the last remote arrivals from rank 0 must land before this CTA exits
@@ -530,25 +689,37 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
   }
 }
 
-// Host-side launcher (bf16 cache).
-cudaError_t launch_decode_bf16(const CUtensorMap& tmap, const DecodeParams& p, int n_pairs, cudaStream_t stream) {
-  auto kern = mla_decode_pair_kernel<0>;
+// Host-side launcher.  kMode 0: bf16 cache through `tmap`; 1: FP8 cache
+// (p.kv_fp8; `tmap` unused).
+template <int kMode>
+cudaError_t launch_decode_mode(const CUtensorMap& tmap, const DecodeParams& p, int n_pairs, cudaStream_t stream) {
+  auto kern = mla_decode_pair_kernel<kMode>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dk::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dk::smem_bytes<kMode>());
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * n_pairs, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = dk::kSmemBytes;
+  cfg.blockDim = dim3(dk::Cfg<kMode>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dk::smem_bytes<kMode>();
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
   return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+}
+
+cudaError_t launch_decode_bf16(const CUtensorMap& tmap, const DecodeParams& p, int n_pairs, cudaStream_t stream) {
+  return launch_decode_mode<0>(tmap, p, n_pairs, stream);
+}
+
+cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, cudaStream_t stream) {
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  return launch_decode_mode<1>(unused, p, n_pairs, stream);
 }
 
 int decode_max_pairs() {
@@ -558,12 +729,12 @@ int decode_max_pairs() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cached_device == dev) return cached;
   auto kern = mla_decode_pair_kernel<0>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dk::kSmemBytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dk::smem_bytes<0>()) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = dk::kSmemBytes;
+  cfg.dynamicSmemBytes = dk::smem_bytes<0>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;

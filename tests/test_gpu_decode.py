@@ -186,3 +186,57 @@ def test_combine_splits_matches_oracle_merge(cuda_device):
             continue
         np.testing.assert_allclose(out[r].double().cpu().numpy(), ro, atol=1e-2 * np.abs(ro).max())
         np.testing.assert_allclose(lse[r].double().cpu().numpy(), rl, atol=1e-5)
+
+
+# ----------------------------------------------------------------- FP8 cache
+def _dequant_bf16(raw: torch.Tensor) -> torch.Tensor:
+    """Oracle dequantisation of [..., 594] rows, cast to bf16 (exact)."""
+    from oracle import fp8_codec
+    return torch.from_numpy(fp8_codec.dequant_rows(raw.numpy())).to(torch.bfloat16)
+
+
+def test_fp8_single_token_is_bit_exact_dequant(cuda_device):
+    inp = gen.make_inputs(8, 1, [1] * 8, kv_dtype="fp8", seed=31)
+    # a wide range of e8m0 exponents (kept where every product is a finite,
+    # normal bf16 number, so the MMA's copy is exact) and the e4m3 extremes
+    scales = [10, 11, 100, 120, 127, 130, 142, 143, 150, 200]
+    for b in range(8):
+        page = int(inp.block_table[b, 0])
+        row = inp.kv_cache[page, 0]
+        row[576:] = torch.tensor([scales[(b + k) % len(scales)] for k in range(18)], dtype=torch.uint8)
+        row[:8] = torch.tensor([0x00, 0x80, 0x01, 0x81, 0x7E, 0xFE, 0x08, 0x77], dtype=torch.uint8)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(8):
+        page = int(inp.block_table[b, 0])
+        want = _dequant_bf16(inp.kv_cache[page, 0])[:512]
+        got = out[b, 0].cpu()
+        assert torch.equal(got.view(torch.int16), want.expand(128, 512).contiguous().view(torch.int16)), b
+
+
+@pytest.mark.parametrize("lens", [[1, 63, 64, 65, 200], [3000, 17]])
+def test_fp8_ragged(cuda_device, lens):
+    inp = gen.make_inputs(len(lens), 1, lens, kv_dtype="fp8", seed=7 + len(lens))
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_fp8_causal_and_unused_nan_codes(cuda_device):
+    lens = [70, 130]
+    inp = gen.make_inputs(2, 2, lens, kv_dtype="fp8", seed=12)
+    ref = oracle(inp)
+    for b, s in enumerate(lens):
+        page = int(inp.block_table[b, (s - 1) // 64])
+        inp.kv_cache[page, s % 64:, :] = 0x7F          # NaN codes past the visible length
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, lse, *ref)
+
+
+def test_fp8_bad_page_sets_status(cuda_device):
+    inp = gen.make_inputs(2, 1, [100, 64], kv_dtype="fp8", seed=4)
+    inp.block_table[1, 0] = -3
+    _, _, st = run_gpu(inp)
+    assert st == -5
