@@ -211,7 +211,9 @@ def test_fp8_single_token_is_bit_exact_dequant(cuda_device):
         page = int(inp.block_table[b, 0])
         want = _dequant_bf16(inp.kv_cache[page, 0])[:512]
         got = out[b, 0].cpu()
-        assert torch.equal(got.view(torch.int16), want.expand(128, 512).contiguous().view(torch.int16)), b
+        # value-exact (the sign of a zero is not kept through the P.V sum,
+        # where masked tokens add +0 to 1 * -0)
+        assert torch.equal(got, want.expand(128, 512)), b
 
 
 @pytest.mark.parametrize("lens", [[1, 63, 64, 65, 200], [3000, 17]])
