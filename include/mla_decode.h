@@ -29,6 +29,8 @@
  *   seq_lens    [B] int32, 0 <= seq_len <= max_pages*64.
  *   out         [B, Sq, 128, 512] bf16      lse [B, Sq, 128] fp32
  *
+ * softmax_scale must be finite and > 0.
+ *
  * Speculative multi-token queries (Multi-Token Prediction, guide section 4):
  * query i of Sq sees the first seq_len - (Sq-1-i) tokens.  A query row that
  * sees no token gets out = 0 and lse = -inf.

@@ -33,13 +33,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // The bf16 cache viewed as a 2-D tensor [num_pages*64 rows, 576 columns],
-// boxes of 64 columns x 64 rows with 128-byte swizzle (one page, one chunk).
-int make_cache_tmap(CUtensorMap* m, const void* cache, int num_pages) {
+// boxes of 64 columns x box_rows rows with 128-byte swizzle.
+int make_cache_tmap(CUtensorMap* m, const void* cache, int num_pages, unsigned box_rows) {
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(num_pages) * kPage};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRow) * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -52,7 +52,8 @@ int validate_common(const void* q_absorbed, const void* q_rope, const void* kv_c
                     int max_pages, float scale, const void* out, const float* lse, const void* workspace) {
   if (!q_absorbed || !q_rope || !kv_cache || !block_table || !seq_lens || !out || !lse || !workspace)
     return MLA_ERR_INVALID_ARG;
-  if (batch < 0 || sq <= 0 || num_pages <= 0 || max_pages <= 0 || !std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || sq <= 0 || num_pages <= 0 || max_pages <= 0 || !std::isfinite(scale) || !(scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || page_size != kPage || sq > kMaxSq) return MLA_ERR_UNSUPPORTED;
   if (static_cast<long long>(batch) * sq > kMaxRows) return MLA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_pages) * kPage >= INT_MAX / 2 ||
@@ -79,9 +80,10 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   const WsLayout L = ws_layout(batch, sq, pairs);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  CUtensorMap tmap;
+  CUtensorMap tmap_k, tmap_v;    // 64-row boxes (score SM), 32-row boxes (value SM)
   if (!fp8) {
-    st = make_cache_tmap(&tmap, kv_cache, num_pages);
+    st = make_cache_tmap(&tmap_k, kv_cache, num_pages, 64);
+    if (st == MLA_OK) st = make_cache_tmap(&tmap_v, kv_cache, num_pages, 32);
     if (st != MLA_OK) return st;
   }
 
@@ -103,7 +105,8 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
   g_prof_before = g_prof_after = nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  const cudaError_t le = fp8 ? launch_decode_fp8(p, ppg * sq, stream) : launch_decode_bf16(tmap, p, ppg * sq, stream);
+  const cudaError_t le =
+      fp8 ? launch_decode_fp8(p, ppg * sq, stream) : launch_decode_bf16(tmap_k, tmap_v, p, ppg * sq, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, stream) != cudaSuccess) return MLA_ERR_CUDA;

@@ -59,3 +59,7 @@ def test_host_validation_without_gpu(lib):
     rc = lib.mla_decode_fp8(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(float("nan")),
                             fake, fake, fake, 1 << 30, z)
     assert rc == -1
+    for bad_scale in (0.0, -0.1):
+        rc = lib.mla_decode_bf16(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(bad_scale),
+                                 fake, fake, fake, 1 << 30, z)
+        assert rc == -1
