@@ -10,33 +10,33 @@
 // the 512-column x 128-lane tensor memory of one SM, so S cannot live beside
 // it.  Each 2-CTA cluster splits the work by role, not by data, and no FLOP
 // is computed twice:
-//   rank 1 ("score SM"): q_absorbed [128 x 512] bf16 resident in TMEM
-//       (256 columns) and q_rope [128 x 64] in a 16 KiB shared tile;
-//       S = Q . K^T for 128-token tiles (two pages) with M=128, N=128, K=576
-//       (32 MMAs with A from TMEM, 4 with A from shared memory) into one of
-//       two 128-column S buffers; K streams through a ring of 16 KiB chunk
-//       slots (128 tokens x 64 columns, 128B swizzle).  N=128 is the
-//       smallest N at which one tcgen05.mma does enough work to hide its
-//       issue cost (N=64 runs at about half the tensor rate).  Four softmax
-//       warps own one head row per thread (row max and sum need no
-//       shuffles), round P to bf16 and send it with st.async into rank 0's
-//       shared memory, page by page, in the 128B-swizzled K-major layout the
-//       MMA reads; the bytes are counted on rank 0's barrier, so no thread
-//       waits for the transfer.
-//   rank 0 ("value SM"): O [128 x 512] fp32 in all 512 TMEM columns,
-//       O += P . V with P (one page, K-major) from shared memory and V read
-//       from 32-token stages as an MN-major operand (two M=128, N=256, K=16
-//       MMAs per 16 tokens); its epilogue warps rescale O when rank 1 moves a
-//       head's reference max and write out = O / l (or an fp32 split partial).
-// Both ranks read every page; the second read is an L2 hit.
-//
-// bf16 cache: the producer warp loads with 2-D TMA (128B swizzle).  FP8
-// cache: the producer bulk-copies raw half pages (32 rows x 594 B) and four
-// dequant warps write the same swizzled bf16 tiles.
+//   rank 1 ("score SM"): Q [128 x 576] bf16 resident in TMEM (288 columns);
+//       per 64-token page S = Q . K^T (36 tcgen05.mma, M=128, N=64, A from
+//       TMEM) into one of two 64-column S buffers; eight softmax warps in two
+//       groups (columns 0..31 and 32..63 of each head row; both take the row
+//       max over all 64 columns, so their reference maxima agree without an
+//       exchange) round P to bf16 and send it with st.async into rank 0's
+//       shared memory in the 128B-swizzled K-major layout its MMA reads; the
+//       bytes are counted on rank 0's barrier, so no thread waits for them.
+//   rank 0 ("value SM"): O [128 x 512] fp32 in all 512 TMEM columns;
+//       O += P . V with P from shared memory and V read from the page tile as
+//       an MN-major operand (two M=128, N=256, K=16 MMAs per 16 tokens); its
+//       epilogue warps rescale O when rank 1 moves a head's reference max and
+//       write out = O / l (or an fp32 split partial).
+// Page loads.  One TMA operation per page per rank: the bf16 cache is
+// described as a 3-D tensor (64 columns, rows, 9 column chunks) with row
+// stride 1152 B and chunk stride 128 B, so a single box of 64 x 64 x 9 (rank
+// 1, 72 KiB) or 64 x 64 x 8 (rank 0, 64 KiB) lands as nine (eight) 128B-
+// swizzled chunks of 64 rows -- exactly the operand layout -- in one copy.
+// An SM's copy engine streams far more bytes per second in large operations
+// than in 8 KiB boxes, so whole-page copies are what lets 152 SMs reach HBM
+// speed.  Both ranks read every page; the second read is an L2 hit.  The FP8
+// cache is bulk-copied as raw half pages and dequantised by four warps into
+// the same layouts.
 //
 // Lazy rescaling: rank 1 keeps a per-head reference max m_ref (raw score
-// units) and moves it only when a tile's max exceeds it by more than 8 in
-// log2 units, so P <= 256 and O is rescaled only on those rare tiles.
+// units) and moves it only when a page's max exceeds it by more than 8 in
+// log2 units, so P <= 256 and O is rescaled only on those rare pages.
 //
 // Every wait is bounded (wait_bounded / wait_warp); a timeout records
 // MLA_STATUS_TIMEOUT and raises an abort flag so every role leaves its loop
@@ -53,54 +53,59 @@ namespace mla {
 
 namespace dk {
 
-constexpr int kTileTok = 128;                          // rank 1 S tile: two pages
-constexpr uint32_t kSlotBytes = kTileTok * 128;        // rank 1 chunk slot: 128 rows x 64 bf16
-constexpr int kVTok = 32;                              // rank 0 V stage: 32 tokens
-constexpr uint32_t kVChunkBytes = kVTok * 128;         // 32 rows x 64 bf16
-constexpr uint32_t kVStageBytes = 8 * kVChunkBytes;    // 32 tokens x 512 columns
-constexpr uint32_t kPSlotBytes = 128 * 128;            // P of one page: 128 heads x 64 tokens bf16
-constexpr int kPSlots = 4;
+constexpr uint32_t kChunkBytes = 64 * 128;            // 64 rows x 64 bf16, 128B swizzle
+constexpr uint32_t kVPageBytes = 8 * kChunkBytes;     // latent c_KV part of one page (64 KiB)
+constexpr uint32_t kPSlotBytes = 128 * 128;           // P of one page: 128 heads x 64 tokens bf16
+constexpr int kPSlots = 2;
 constexpr int kMailSlots = 2;
-constexpr uint32_t kRawBytes = 32 * kFp8Row;           // half a page of FP8 rows: 19,008 B
-constexpr int kMaxSlots = 12, kMaxRaw = 6;
+constexpr uint32_t kRawBytes = 32 * kFp8Row;          // half a page of FP8 rows: 19,008 B
+constexpr int kMaxStages = 3, kMaxRaw = 4;
 
-// Shared-memory plans (bytes).  Rank 1: q_rope tile, chunk-slot ring, raw
-// ring (FP8).  Rank 0: V-stage ring, P slots, raw ring (FP8).  The small
-// common region (alpha, 1/l, flags, barriers) sits at the same offset in both
-// ranks so remote stores and arrivals can address it.
+// Shared-memory plans (bytes).  The small common region (alpha, 1/l, flags,
+// barriers) sits at the same offset in both ranks so remote stores and
+// arrivals can address it.
+//   bf16: rank 1 = 3 K pages of 72 KiB (chunks 0..8 contiguous);
+//         rank 0 = 3 V pages of 64 KiB + 2 P slots.
+//   FP8:  rank 1 = 2 bf16 K pages (latent chunks at stage*64K, RoPE chunk in
+//         a separate ring) + 4 raw half pages; rank 0 = 2 V pages + 2 P slots
+//         + 3 raw half pages.
 template <int kMode> struct Cfg;
-template <> struct Cfg<0> {            // bf16 cache: 2-D TMA tiles
-  static constexpr int kSlots1 = 12, kVStages0 = 4, kRaw1 = 0, kRaw0 = 0;
-  static constexpr uint32_t kOffQR = 0;
-  static constexpr uint32_t kOffSlots = 16384;
-  static constexpr uint32_t kOffRaw1 = 0;
-  static constexpr uint32_t kOffV = 0;
-  static constexpr uint32_t kOffP = kVStages0 * kVStageBytes;
-  static constexpr uint32_t kOffRaw0 = 0;
-  static constexpr uint32_t kOffMisc = kOffSlots + kSlots1 * kSlotBytes;
-  static constexpr int kThreads = 256;
+template <> struct Cfg<0> {
+  static constexpr int kStages = 3;
+  static constexpr int kRaw1 = 0, kRaw0 = 0;
+  static constexpr uint32_t kKStageBytes = 9 * kChunkBytes;
+  static constexpr uint32_t kOffRope = 0;                           // unused: RoPE chunk is chunk 8 of the stage
+  static constexpr uint32_t kOffP = kStages * kVPageBytes;
+  static constexpr uint32_t kOffRaw1 = 0, kOffRaw0 = 0;
+  static constexpr uint32_t kOffMisc = kOffP + kPSlots * kPSlotBytes;
+  static constexpr int kThreads = 384;
+  __device__ static uint32_t k_chunk(int stage, int c) { return stage * kKStageBytes + c * kChunkBytes; }
 };
-template <> struct Cfg<1> {            // FP8 cache: bulk copies + dequant warps 8..11
-  static constexpr int kSlots1 = 6, kVStages0 = 3, kRaw1 = 6, kRaw0 = 3;
-  static constexpr uint32_t kOffQR = 0;
-  static constexpr uint32_t kOffSlots = 16384;
-  static constexpr uint32_t kOffRaw1 = kOffSlots + kSlots1 * kSlotBytes;
-  static constexpr uint32_t kOffV = 0;
-  static constexpr uint32_t kOffP = kVStages0 * kVStageBytes;
+template <> struct Cfg<1> {
+  static constexpr int kStages = 2;
+  static constexpr int kRaw1 = 4, kRaw0 = 3;
+  static constexpr uint32_t kKStageBytes = kVPageBytes;
+  static constexpr uint32_t kOffRope = kStages * kVPageBytes;       // rank 1: RoPE chunk ring
+  static constexpr uint32_t kOffP = kStages * kVPageBytes;          // rank 0: P slots
+  static constexpr uint32_t kOffRaw1 = kOffRope + kStages * kChunkBytes;
   static constexpr uint32_t kOffRaw0 = kOffP + kPSlots * kPSlotBytes;
   static constexpr uint32_t kOffMisc = kOffRaw1 + kRaw1 * kRawBytes;
-  static constexpr int kThreads = 384;
+  static constexpr int kThreads = 512;
+  __device__ static uint32_t k_chunk(int stage, int c) {
+    return c < 8 ? stage * kVPageBytes + c * kChunkBytes : kOffRope + stage * kChunkBytes;
+  }
 };
-constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [4][128]
-constexpr uint32_t kMiscMail = 2048;     // rank 0: fp32 1/l [2][128]
-constexpr uint32_t kMiscReq = 3072;      // rank 0: P slot of a rescale request
-constexpr uint32_t kMiscRawFlag = 3088;  // per raw stage: 1 = write zeros (bad or absent page)
-constexpr uint32_t kMiscBar = 3136;
+constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
+constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
+constexpr uint32_t kMiscMail = 1024;     // rank 0: fp32 1/l [2][128]
+constexpr uint32_t kMiscReq = 2048;      // rank 0: P slot of a rescale request
+constexpr uint32_t kMiscRawFlag = 2064;  // per raw stage: 1 = write zeros (bad page)
+constexpr uint32_t kMiscBar = 2080;
 enum Bar {
-  FULL = 0, EMPTY = FULL + kMaxSlots,
-  PFULL = EMPTY + kMaxSlots, PEMPTY = PFULL + kPSlots,
+  FULL = 0, EMPTY = FULL + kMaxStages,
+  PFULL = EMPTY + kMaxStages, PEMPTY = PFULL + kPSlots,
   SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + 2,
-  QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY,
+  QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY, LSUM,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
   RAWFULL = MBEMPTY + kMailSlots, RAWEMPTY = RAWFULL + kMaxRaw,
   NBAR = RAWEMPTY + kMaxRaw
@@ -109,16 +114,15 @@ constexpr uint32_t kMiscTmem = kMiscBar + NBAR * 8;
 constexpr uint32_t kMiscBytes = kMiscTmem + 16;
 template <int kMode> constexpr uint32_t smem_bytes() { return Cfg<kMode>::kOffMisc + kMiscBytes; }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory budget");
-static_assert(Cfg<0>::kOffP + kPSlots * kPSlotBytes <= Cfg<0>::kOffMisc, "rank 0 plan (bf16)");
+static_assert(3 * 9 * kChunkBytes <= Cfg<0>::kOffMisc, "rank 1 plan (bf16)");
 static_assert(Cfg<1>::kOffRaw0 + Cfg<1>::kRaw0 * kRawBytes <= Cfg<1>::kOffMisc, "rank 0 plan (fp8)");
-static_assert(Cfg<0>::kSlots1 <= kMaxSlots && Cfg<1>::kRaw1 <= kMaxRaw, "barrier arrays");
 
 // TMEM columns.
-constexpr uint32_t kQCol = 0;       // rank 1: q_absorbed, 256 columns (2 bf16 per column)
-constexpr uint32_t kSCol = 256;     // rank 1: two S buffers of 128 columns
+constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
+constexpr uint32_t kSCol = 320;    // rank 1: two S buffers of 64 columns
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescS = ptx::idesc_bf16(128, 128, 0, 0);   // A = Q (K-major), B = K (K-major)
+constexpr uint32_t kIdescS = ptx::idesc_bf16(128, 64, 0, 0);    // A = Q (TMEM, K-major), B = K (K-major)
 constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 256, 0, 1);  // A = P (K-major), B = V (MN-major)
 
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -226,6 +230,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                        const DecodeParams p) {
   using namespace dk;
   using C = Cfg<kMode>;
+  constexpr int kStages = C::kStages;
   constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
   constexpr uint32_t kOffMail = C::kOffMisc + kMiscMail;
   constexpr uint32_t kOffReq = C::kOffMisc + kMiscReq;
@@ -250,31 +255,27 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const bool smem_ok = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
     if (!smem_ok) set_status(&hdr->status, MLA_ERR_UNSUPPORTED);
-    const uint32_t full_count = kMode == 0 ? 1u : 4u;     // TMA bytes, or the 4 dequant warps
-    for (int s = 0; s < kMaxSlots; ++s) { ptx::mbar_init(BAR(FULL + s), full_count); ptx::mbar_init(BAR(EMPTY + s), 1); }
-    for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128); ptx::mbar_init(BAR(PEMPTY + s), 1); }
-    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128); }
+    for (int s = 0; s < kMaxStages; ++s) {
+      ptx::mbar_init(BAR(FULL + s), kMode == 0 ? 1u : 4u);   // TMA bytes, or the 4 dequant warps
+      ptx::mbar_init(BAR(EMPTY + s), 1);
+    }
+    for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 256); ptx::mbar_init(BAR(PEMPTY + s), 1); }
+    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 256); }
     ptx::mbar_init(BAR(QREADY), 128);
     ptx::mbar_init(BAR(REQ), 2);
     ptx::mbar_init(BAR(CORR), 4);
     ptx::mbar_init(BAR(OFULL), 1);
     ptx::mbar_init(BAR(OEMPTY), 128);
+    ptx::mbar_init(BAR(LSUM), 128);
     for (int s = 0; s < kMailSlots; ++s) { ptx::mbar_init(BAR(MBFULL + s), 128); ptx::mbar_init(BAR(MBEMPTY + s), 4); }
-    // rank 1 gives each raw half page to one dequant warp; rank 0 to all four
-    for (int s = 0; s < kMaxRaw; ++s) {
-      ptx::mbar_init(BAR(RAWFULL + s), 1);
-      ptx::mbar_init(BAR(RAWEMPTY + s), rank == 1 ? 1u : 4u);
-    }
+    for (int s = 0; s < kMaxRaw; ++s) { ptx::mbar_init(BAR(RAWFULL + s), 1); ptx::mbar_init(BAR(RAWEMPTY + s), 4); }
     ptx::fence_barrier_init();
   }
   if (warp == 2) {
     ptx::tmem_alloc(sbase + kOffTmemPtr, kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (kMode == 0 && warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tmap_k);
-    ptx::prefetch_tmap(&tmap_v);
-  }
+  if (kMode == 0 && warp == 0 && lane == 0) ptx::prefetch_tmap(rank == 1 ? &tmap_k : &tmap_v);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -292,215 +293,133 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const bool active = smem_ok && group < sq;
 
   if (active && warp == 0) {
-    // ------------------------------------------------------------ producers
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_normal();
       SegWalker w; w.init(tile_start, p.batch, lo, hi);
       Segment sg;
-      int slot = 0; uint32_t sphase = 0;
+      int stage = 0; uint32_t phase = 0;
       int rs = 0; uint32_t rphase = 0;
-      const int n_slots = rank == 1 ? C::kSlots1 : C::kVStages0;
       const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
       const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
       volatile uint32_t* raw_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffRawFlag);
-      auto page_of = [&](int b, int t, bool& bad) -> int {
-        int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + t);
-        bad = pg < 0 || pg >= p.num_pages;
-        if (bad) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
-        return pg;
-      };
-      // FP8: one raw half page (or zeros for a bad or absent page)
-      auto load_raw = [&](int page, bool zero, int half) -> bool {
-        if (!wait_bounded<true>(BAR(RAWEMPTY + rs), rphase ^ 1u, hdr)) return false;
-        raw_flag[rs] = zero ? 1u : 0u;
-        if (zero) {
-          ptx::mbar_arrive(BAR(RAWFULL + rs));
-        } else {
-          ptx::mbar_arrive_expect_tx(BAR(RAWFULL + rs), kRawBytes);
-          const uint8_t* src = p.kv_fp8 + static_cast<size_t>(page) * (kPage * kFp8Row) + half * kRawBytes;
-          ptx::bulk_load(sbase + raw_off + static_cast<uint32_t>(rs) * kRawBytes, src, kRawBytes,
-                         BAR(RAWFULL + rs), pol);
-        }
-        if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
-        return true;
-      };
       bool ok = true;
       while (ok && w.next(sg)) {
-        if (rank == 1) {
-          // 128-token tiles: pages (t, t+1); nine 16 KiB chunk slots per tile
-          for (int t = sg.t0; t < sg.t1 && ok; t += 2) {
-            bool bad_a = false, bad_b = false;
-            const int pa = page_of(sg.b, t, bad_a);
-            const bool has_b = t + 1 < sg.t1;
-            const int pb = has_b ? page_of(sg.b, t + 1, bad_b) : 0;
-            if constexpr (kMode == 0) {
-              // a bad or absent page is read fully outside the tensor: zeros
-              const int ya = (bad_a ? p.num_pages : pa) * kPage;
-              const int yb = (!has_b || bad_b ? p.num_pages : pb) * kPage;
-              for (int c = 0; c < 9; ++c) {
-                if (!wait_bounded<true>(BAR(EMPTY + slot), sphase ^ 1u, hdr)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(BAR(FULL + slot), kSlotBytes);
-                const uint32_t dst = sbase + C::kOffSlots + static_cast<uint32_t>(slot) * kSlotBytes;
-                ptx::tma_load_2d(dst, &tmap_k, BAR(FULL + slot), c * 64, ya, pol);
-                ptx::tma_load_2d(dst + kSlotBytes / 2, &tmap_k, BAR(FULL + slot), c * 64, yb, pol);
-                if (++slot == n_slots) { slot = 0; sphase ^= 1u; }
-              }
+        for (int t = sg.t0; t < sg.t1 && ok; ++t) {
+          int page = __ldg(p.block_table + static_cast<size_t>(sg.b) * p.max_pages + t);
+          const bool bad = page < 0 || page >= p.num_pages;
+          if (bad) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
+          if constexpr (kMode == 0) {
+            // one copy per page: rank 1 all nine chunks (72 KiB), rank 0 the
+            // eight latent chunks (64 KiB); a bad page is read fully outside
+            // the tensor, which fills zeros
+            if (!wait_bounded<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
+            const int y = (bad ? p.num_pages : page) * kPage;
+            if (rank == 1) {
+              ptx::mbar_arrive_expect_tx(BAR(FULL + stage), 9u * kChunkBytes);
+              ptx::tma_load_3d(sbase + C::k_chunk(stage, 0), &tmap_k, BAR(FULL + stage), 0, y, 0, pol);
             } else {
-              for (int hp = 0; hp < 4 && ok; ++hp) {
-                const bool is_b = hp >= 2;
-                const bool zero = is_b ? (!has_b || bad_b) : bad_a;
-                ok = load_raw(is_b ? pb : pa, zero, hp & 1);
-              }
+              ptx::mbar_arrive_expect_tx(BAR(FULL + stage), kVPageBytes);
+              ptx::tma_load_3d(sbase + static_cast<uint32_t>(stage) * kVPageBytes, &tmap_v, BAR(FULL + stage),
+                               0, y, 0, pol);
             }
-          }
-        } else {
-          // pages, each as two 32-token V stages
-          for (int t = sg.t0; t < sg.t1 && ok; ++t) {
-            bool bad = false;
-            const int pg = page_of(sg.b, t, bad);
-            for (int half = 0; half < 2 && ok; ++half) {
-              if constexpr (kMode == 0) {
-                if (!wait_bounded<true>(BAR(EMPTY + slot), sphase ^ 1u, hdr)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(BAR(FULL + slot), kVStageBytes);
-                const int y = (bad ? p.num_pages * kPage : pg * kPage + half * kVTok);
-                const uint32_t dst = sbase + C::kOffV + static_cast<uint32_t>(slot) * kVStageBytes;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  ptx::tma_load_2d(dst + c * kVChunkBytes, &tmap_v, BAR(FULL + slot), c * 64, y, pol);
-                if (++slot == n_slots) { slot = 0; sphase ^= 1u; }
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          } else {
+            // two raw half pages; a bad page is never read (dequant writes zeros)
+            for (int half = 0; half < 2; ++half) {
+              if (!wait_bounded<true>(BAR(RAWEMPTY + rs), rphase ^ 1u, hdr)) { ok = false; break; }
+              raw_flag[rs] = bad ? 1u : 0u;
+              if (bad) {
+                ptx::mbar_arrive(BAR(RAWFULL + rs));
               } else {
-                ok = load_raw(pg, bad, half);
+                ptx::mbar_arrive_expect_tx(BAR(RAWFULL + rs), kRawBytes);
+                const uint8_t* src = p.kv_fp8 + static_cast<size_t>(page) * (kPage * kFp8Row) + half * kRawBytes;
+                ptx::bulk_load(sbase + raw_off + static_cast<uint32_t>(rs) * kRawBytes, src, kRawBytes,
+                               BAR(RAWFULL + rs), pol);
               }
+              if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
             }
           }
         }
       }
     }
-  } else if (kMode == 1 && active && warp >= 8 && rank == 1) {
-    // ------------------------------------------------------------ FP8 dequant, rank 1
-    // Warp wq owns raw half page wq of the tile (rows 32*wq .. 32*wq+31 of
-    // every chunk slot); lane = row; chunk c takes value groups 2c, 2c+1.
-    const int wq = warp - 8;
+  } else if (kMode == 1 && active && warp >= 12) {
+    // ------------------------------------------------------------ FP8 dequant (warps 12..15)
+    // raw half page -> bf16 operand rows [32*half, 32*half+32) of the page.
+    // Warp wq handles tokens of parity (wq & 1) (so the row's 2-byte
+    // misalignment is warp-uniform) and half of the 32-value groups (9 of 18
+    // on rank 1, 8 of the 16 latent groups on rank 0).
+    const int wq = warp - 12;
+    const int parity = wq & 1;
+    const int G = rank == 1 ? 9 : 8;
+    const int g0 = (wq >> 1) * G;
+    const int n_tasks = 16 * G;
+    const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
+    const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
     const volatile uint32_t* raw_flag = reinterpret_cast<const volatile uint32_t*>(smem + kOffRawFlag);
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int slot = 0; uint32_t sphase = 0;
-    int rs = 0; uint32_t rphase = 0;      // first raw stage of the current tile
-    bool ok = true;
-    while (ok && w.next(sg)) {
-      for (int t = sg.t0; t < sg.t1 && ok; t += 2) {
-        int my = rs + wq; uint32_t my_phase = rphase;
-        if (my >= C::kRaw1) { my -= C::kRaw1; my_phase ^= 1u; }
-        if (!wait_warp<false>(BAR(RAWFULL + my), my_phase, hdr)) { ok = false; break; }
-        const bool zero = raw_flag[my] != 0;
-        const uint8_t* row = smem + C::kOffRaw1 + static_cast<uint32_t>(my) * kRawBytes + lane * kFp8Row;
-        for (int c = 0; c < 9; ++c) {
-          if (!wait_warp<true>(BAR(EMPTY + slot), sphase ^ 1u, hdr)) { ok = false; break; }
-          uint8_t* dst = smem + C::kOffSlots + static_cast<uint32_t>(slot) * kSlotBytes;
-          const int r = 32 * wq + lane;
-#pragma unroll
-          for (int gg = 0; gg < 2; ++gg) {
-            const int g = 2 * c + gg;
-            uint32_t o[16];
-            if (!zero) {
-              dequant_group(row, g, o);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = 0u;
-            }
-            store_group(dst, r, g, o);
-          }
-          ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA (async proxy)
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(BAR(FULL + slot));
-          if (++slot == C::kSlots1) { slot = 0; sphase ^= 1u; }
-        }
-        if (!ok) break;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(BAR(RAWEMPTY + my));
-        rs += 4;
-        if (rs >= C::kRaw1) { rs -= C::kRaw1; rphase ^= 1u; }
-      }
-    }
-  } else if (kMode == 1 && active && warp >= 8 && rank == 0) {
-    // ------------------------------------------------------------ FP8 dequant, rank 0
-    // One raw half page -> one 32-token V stage; thread t: token t/4, groups
-    // (t%4) + 4i of the 16 latent groups.
-    const int dt = threadIdx.x - 256;
-    const int tok = dt >> 2, gq = dt & 3;
-    const volatile uint32_t* raw_flag = reinterpret_cast<const volatile uint32_t*>(smem + kOffRawFlag);
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
-    Segment sg;
-    int slot = 0; uint32_t sphase = 0;
+    int stage = 0; uint32_t phase = 0;
     int rs = 0; uint32_t rphase = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
       for (int t = sg.t0; t < sg.t1 && ok; ++t) {
+        if (!wait_warp<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
         for (int half = 0; half < 2; ++half) {
-          if (!wait_warp<true>(BAR(EMPTY + slot), sphase ^ 1u, hdr) ||
-              !wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
+          if (!wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
           const bool zero = raw_flag[rs] != 0;
-          const uint8_t* row = smem + C::kOffRaw0 + static_cast<uint32_t>(rs) * kRawBytes + tok * kFp8Row;
-          uint8_t* stage = smem + C::kOffV + static_cast<uint32_t>(slot) * kVStageBytes;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int g = gq + 4 * i;
+          const uint8_t* raw = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes;
+          for (int task = lane; task < n_tasks; task += 32) {
+            const int tok = 2 * (task / G) + parity;          // token within the half page
+            const int g = g0 + task % G;                       // 32-value group
             uint32_t o[16];
             if (!zero) {
-              dequant_group(row, g, o);
+              dequant_group(raw + tok * kFp8Row, g, o);
             } else {
 #pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] = 0u;
+              for (int i = 0; i < 16; ++i) o[i] = 0u;
             }
-            store_group(stage + (g >> 1) * kVChunkBytes, tok, g, o);
+            store_group(smem + C::k_chunk(stage, g >> 1), 32 * half + tok, g, o);
           }
-          ptx::fence_proxy_async_cta();
+          ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA (async proxy)
           __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(BAR(RAWEMPTY + rs));
-            ptx::mbar_arrive(BAR(FULL + slot));
-          }
-          if (++rs == C::kRaw0) { rs = 0; rphase ^= 1u; }
-          if (++slot == C::kVStages0) { slot = 0; sphase ^= 1u; }
+          if (lane == 0) ptx::mbar_arrive(BAR(RAWEMPTY + rs));
+          if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
         }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(BAR(FULL + stage));
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (active && warp == 1 && rank == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int slot = 0; uint32_t phase = 0;
+    int stage = 0; uint32_t phase = 0;
     int sb = 0; uint32_t sphase = 0;
     uint32_t qphase = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
       if (!wait_warp<false>(BAR(QREADY), qphase, hdr)) break;
       qphase ^= 1u;
-      for (int t = sg.t0; t < sg.t1 && ok; t += 2) {
-        if (!wait_warp<false>(BAR(SEMPTY + sb), sphase ^ 1u, hdr)) { ok = false; break; }
-        const uint32_t d = tmem + kSCol + 128u * sb;
-        for (int c = 0; c < 9; ++c) {
-          if (!wait_warp<false>(BAR(FULL + slot), phase, hdr)) { ok = false; break; }
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            const uint32_t bbase = sbase + C::kOffSlots + static_cast<uint32_t>(slot) * kSlotBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bdesc = ptx::sdesc_sw128(bbase + kk * 32, 16, 1024);
-              const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-              if (c < 8) {
-                ptx::mma_ts(d, tmem + kQCol + 8u * (4 * c + kk), bdesc, kIdescS, acc);
-              } else {
-                const uint64_t adesc = ptx::sdesc_sw128(sbase + C::kOffQR + kk * 32, 16, 1024);
-                ptx::mma_ss(d, adesc, bdesc, kIdescS, acc);
-              }
-            }
-            ptx::mma_commit(BAR(EMPTY + slot));
-            if (c == 8) ptx::mma_commit(BAR(SFULL + sb));
+      for (int t = sg.t0; t < sg.t1 && ok; ++t) {
+        if (!wait_warp<false>(BAR(FULL + stage), phase, hdr) ||
+            !wait_warp<false>(BAR(SEMPTY + sb), sphase ^ 1u, hdr)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + kSCol + 64u * sb;
+#pragma unroll 4
+          for (int k = 0; k < kRow / 16; ++k) {
+            const uint32_t baddr = sbase + C::k_chunk(stage, k >> 2) + (k & 3) * 32;
+            const uint64_t bdesc = ptx::sdesc_sw128(baddr, 16, 1024);
+            ptx::mma_ts(d, tmem + kQCol + 8u * k, bdesc, kIdescS, k > 0 ? 1u : 0u);
           }
-          __syncwarp();
-          if (++slot == C::kSlots1) { slot = 0; phase ^= 1u; }
+          ptx::mma_commit(BAR(EMPTY + stage));
+          ptx::mma_commit(BAR(SFULL + sb));
         }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
       }
     }
@@ -508,7 +427,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     // ------------------------------------------------------------ O += P V issuer
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int slot = 0; uint32_t phase = 0;
+    int stage = 0; uint32_t phase = 0;
     int ps = 0; uint32_t pphase = 0;
     uint32_t corr_phase = 0, oe_phase = 0;
     bool first_seg = true, ok = true;
@@ -517,9 +436,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     while (ok && w.next(sg)) {
       const int len_i = lens[sg.b] - (sq - 1 - group);
       for (int t = sg.t0; t < sg.t1 && ok; ++t) {
-        if (!wait_warp<true>(BAR(PFULL + ps), pphase, hdr)) { ok = false; break; }
+        if (!wait_warp<false>(BAR(FULL + stage), phase, hdr) ||
+            !wait_warp<true>(BAR(PFULL + ps), pphase, hdr)) { ok = false; break; }
         ptx::fence_proxy_async_cta();
-        // did rank 1 move its reference max for any head on this page?
+        // did rank 1 move its reference max for any head of this page?
         bool moved = false;
 #pragma unroll
         for (int i = 0; i < 4; ++i) moved |= alpha_buf[ps * 128 + lane * 4 + i] != 1.f;
@@ -538,113 +458,111 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           if (!wait_warp<false>(BAR(OEMPTY), oe_phase, hdr)) { ok = false; break; }
           oe_phase ^= 1u;
         }
-        for (int half = 0; half < 2; ++half) {
-          if (!wait_warp<false>(BAR(FULL + slot), phase, hdr)) { ok = false; break; }
-          const int valid = len_i - (t * kPage + half * kVTok);   // rows visible to the query
-          if (valid < kVTok) {
-            // rows past the visible length get P = 0; make their V finite too
-            const int v0 = valid > 0 ? valid : 0;
-            uint4* base = reinterpret_cast<uint4*>(smem + C::kOffV + static_cast<uint32_t>(slot) * kVStageBytes);
-            const int n16 = (kVTok - v0) * 8;     // 16-byte pieces per chunk
-            for (int c = 0; c < 8; ++c)
-              for (int i = lane; i < n16; i += 32)
-                base[(c * kVChunkBytes + v0 * 128) / 16 + i] = make_uint4(0, 0, 0, 0);
-            ptx::fence_proxy_async_cta();
-            __syncwarp();
-          }
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            const uint32_t pbase = sbase + C::kOffP + static_cast<uint32_t>(ps) * kPSlotBytes;
-            const uint32_t vbase = sbase + C::kOffV + static_cast<uint32_t>(slot) * kVStageBytes;
-#pragma unroll
-            for (int k = 0; k < kVTok / 16; ++k) {
-              const uint64_t adesc = ptx::sdesc_sw128(pbase + (half * 2 + k) * 32, 16, 1024);
-#pragma unroll
-              for (int n = 0; n < 2; ++n) {
-                const uint64_t bdesc =
-                    ptx::sdesc_sw128(vbase + n * 4 * kVChunkBytes + k * 2048, kVChunkBytes, 1024);
-                ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV,
-                            (t > sg.t0 || half > 0 || k > 0) ? 1u : 0u);
-              }
-            }
-            ptx::mma_commit(BAR(EMPTY + slot));
-            if (half == 1) {
-              ptx::mma_commit_mc(BAR(PEMPTY + ps), static_cast<uint16_t>(1u << 1));
-              if (t == sg.t1 - 1) ptx::mma_commit(BAR(OFULL));
-            }
-          }
+        const uint32_t vpage = static_cast<uint32_t>(stage) * kVPageBytes;
+        const int valid = len_i - t * kPage;   // rows of this page visible to the query
+        if (valid < kPage) {
+          // rows past the visible length get P = 0; make their V finite too
+          const int v0 = valid > 0 ? valid : 0;
+          uint4* base = reinterpret_cast<uint4*>(smem + vpage);
+          const int n16 = (kPage - v0) * 8;     // 16-byte pieces per chunk
+          for (int c = 0; c < 8; ++c)
+            for (int i = lane; i < n16; i += 32)
+              base[(c * kChunkBytes + v0 * 128) / 16 + i] = make_uint4(0, 0, 0, 0);
+          ptx::fence_proxy_async_cta();
           __syncwarp();
-          if (++slot == C::kVStages0) { slot = 0; phase ^= 1u; }
         }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t pbase = sbase + C::kOffP + static_cast<uint32_t>(ps) * kPSlotBytes;
+          const uint32_t vbase = sbase + vpage;
+#pragma unroll
+          for (int k = 0; k < kPage / 16; ++k) {
+            const uint64_t adesc = ptx::sdesc_sw128(pbase + k * 32, 16, 1024);
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              const uint64_t bdesc = ptx::sdesc_sw128(vbase + n * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024);
+              ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, (t > sg.t0 || k > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(BAR(EMPTY + stage));
+          ptx::mma_commit_mc(BAR(PEMPTY + ps), static_cast<uint16_t>(1u << 1));
+          if (t == sg.t1 - 1) ptx::mma_commit(BAR(OFULL));
+        }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
       first_seg = false;
     }
-  } else if (active && warp >= 4 && warp < 8 && rank == 1) {
+  } else if (active && warp >= 4 && warp < 12 && rank == 1) {
     // ------------------------------------------------------------ softmax (thread = head)
-    const int h = threadIdx.x - 128;
+    // Group 0 (warps 4..7) turns columns 0..31 of each page's S into P, group
+    // 1 (warps 8..11) columns 32..63.  Both take the row max over all 64
+    // columns, so their reference maxima and rescale factors agree without an
+    // exchange; the two partial sums meet once per segment (LSUM barrier).
+    const int grp = (warp - 4) >> 2;
+    const int h = (threadIdx.x - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    volatile float* l_part = reinterpret_cast<volatile float*>(smem + C::kOffMisc + kMiscLPart);
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
     int sb = 0; uint32_t sphase = 0;
     int ps = 0; uint32_t pphase = 0;
     int ms = 0; uint32_t mphase = 0;
+    uint32_t lsum_phase = 0;
     bool ok = true;
     const float c = p.scale_log2;
     while (ok && w.next(sg)) {
       const int row = sg.b * sq + group;
       const int len_i = lens[sg.b] - (sq - 1 - group);
-      const int seg_end = min(len_i, sg.t1 * kPage);       // tokens of this segment visible to the query
-      // q_absorbed row h -> TMEM lane h (two bf16 per column, K order);
-      // q_rope row h -> shared tile (128B-swizzled K-major, 128 B per head)
-      {
+      if (grp == 0) {
+        // Q row h -> TMEM lane h, columns [0, 288): two bf16 per column, K order
         const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<size_t>(row) * kHeads + h) * kDc);
         const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + (static_cast<size_t>(row) * kHeads + h) * kDr);
-        uint4 x[8];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) x[v] = __ldg(qr + v);
-        uint8_t* qr_row = smem + C::kOffQR + h * 128;
-#pragma unroll
-        for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(qr_row + ((v ^ (h & 7)) << 4)) = x[v];
 #pragma unroll 1
-        for (int qq = 0; qq < 4; ++qq) {      // 2 chunks of 32 columns per round trip
-          uint4 y[16];
+        for (int c3 = 0; c3 < 3; ++c3) {          // three chunks of 32 columns per round trip
+          uint4 x[24];
 #pragma unroll
-          for (int v = 0; v < 16; ++v) y[v] = __ldg(qa + qq * 16 + v);
+          for (int v = 0; v < 24; ++v) {
+            const int cc = c3 * 3 + v / 8;
+            x[v] = __ldg((cc < 8 ? qa + cc * 8 : qr) + (v & 7));
+          }
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
+          for (int j = 0; j < 3; ++j) {
             uint32_t r[32];
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-              r[4 * v] = y[8 * j + v].x; r[4 * v + 1] = y[8 * j + v].y;
-              r[4 * v + 2] = y[8 * j + v].z; r[4 * v + 3] = y[8 * j + v].w;
+              r[4 * v] = x[8 * j + v].x; r[4 * v + 1] = x[8 * j + v].y;
+              r[4 * v + 2] = x[8 * j + v].z; r[4 * v + 3] = x[8 * j + v].w;
             }
-            ptx::tmem_st32(tmem + lane_base + kQCol + 32u * (qq * 2 + j), r);
+            ptx::tmem_st32(tmem + lane_base + kQCol + 32u * (c3 * 3 + j), r);
           }
         }
-        ptx::fence_proxy_async_cta();
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(BAR(QREADY));
       }
       float m_ref = -INFINITY, l = 0.f;
-      for (int t = sg.t0; t < sg.t1; t += 2) {
+      for (int t = sg.t0; t < sg.t1; ++t) {
         if (!wait_warp<false>(BAR(SFULL + sb), sphase, hdr)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t sadr = tmem + lane_base + kSCol + 128u * sb;
-        const int valid = seg_end - t * kPage;    // columns of this tile visible to the query
-        // pass 1: row max of the masked raw scores.  m_ref stays in raw score
-        // units and P = exp2((s - m_ref) * c), so the max element gets exactly
-        // exp2(0) = 1 whatever the magnitude of the scores (scale c > 0).
+        const uint32_t sadr = tmem + lane_base + kSCol + 64u * sb;
+        uint32_t mine[32], other[32];
+        ptx::tmem_ld32(sadr + 32u * grp, mine);
+        ptx::tmem_ld32(sadr + 32u * (grp ^ 1), other);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(BAR(SEMPTY + sb));
+        const int valid = len_i - t * kPage;          // columns of this page visible to the query
+        const int c_mine = 32 * grp, c_other = 32 * (grp ^ 1);
+        // row max of the masked raw scores.  m_ref stays in raw score units and
+        // P = exp2((s - m_ref) * c), so the max element gets exactly exp2(0) = 1
+        // whatever the magnitude of the scores (scale c > 0).
         float mx = -INFINITY;
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t r[32];
-          ptx::tmem_ld32(sadr + 32u * q4, r);
-          ptx::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * q4 + e < valid) mx = fmaxf(mx, __uint_as_float(r[e]));
+        for (int e = 0; e < 32; ++e) {
+          if (c_mine + e < valid) mx = fmaxf(mx, __uint_as_float(mine[e]));
+          if (c_other + e < valid) mx = fmaxf(mx, __uint_as_float(other[e]));
         }
         float alpha = 1.f;
         if (t == sg.t0) {
@@ -654,61 +572,57 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           l *= alpha;
           m_ref = mx;
         }
-        // pass 2: P = exp2((s - m_ref) * c) in bf16, page by page to rank 0
-        const int n_pages = t + 1 < sg.t1 ? 2 : 1;
-        for (int pg = 0; pg < n_pages; ++pg) {
-          uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            uint32_t r[32];
-            ptx::tmem_ld32(sadr + 64u * pg + 32u * q2, r);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int col = 64 * pg + 32 * q2 + 2 * e;
-              const float p0 = col < valid ? fast_exp2((__uint_as_float(r[2 * e]) - m_ref) * c) : 0.f;
-              const float p1 = col + 1 < valid ? fast_exp2((__uint_as_float(r[2 * e + 1]) - m_ref) * c) : 0.f;
-              pk[16 * q2 + e] = pack_bf16x2(p0, p1);
-              l += p0 + p1;
-            }
-          }
-          if (pg == n_pages - 1) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(BAR(SEMPTY + sb));
-          }
-          if (!wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr)) { ok = false; break; }
-          // P row h (128 B, swizzled) and alpha go to rank 0 as st.async bytes
-          // counted on its PFULL barrier: nobody waits for them here.
-          const uint32_t pfull = ptx::mapa(BAR(PFULL + ps), 0);
-          ptx::mbar_arrive_expect_tx_remote(pfull, 8u * 16u + 4u);
-          const uint32_t prow = ptx::mapa(sbase + C::kOffP + static_cast<uint32_t>(ps) * kPSlotBytes + h * 128u, 0);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ptx::st_async_v4(prow + ((j ^ (h & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3],
-                             pfull);
-          ptx::st_async_b32(ptx::mapa(sbase + kOffAlpha + ps * 512u + h * 4u, 0),
-                            __float_as_uint(pg == 0 ? alpha : 1.f), pfull);
-          if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
+        for (int e = 0; e < 16; ++e) {
+          const int col = c_mine + 2 * e;
+          const float p0 = col < valid ? fast_exp2((__uint_as_float(mine[2 * e]) - m_ref) * c) : 0.f;
+          const float p1 = col + 1 < valid ? fast_exp2((__uint_as_float(mine[2 * e + 1]) - m_ref) * c) : 0.f;
+          pk[e] = pack_bf16x2(p0, p1);
+          l += p0 + p1;
         }
-        if (!ok) break;
         if (m_ref == -INFINITY) l = 0.f;     // nothing visible yet (every p was 0)
+        if (!wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr)) { ok = false; break; }
+        // This group's half of P row h (64 B, swizzled) -- and, from group 0,
+        // alpha_h -- go to rank 0 as st.async bytes counted on its PFULL
+        // barrier: nobody waits for them here.
+        const uint32_t pfull = ptx::mapa(BAR(PFULL + ps), 0);
+        ptx::mbar_arrive_expect_tx_remote(pfull, grp == 0 ? 4u * 16u + 4u : 4u * 16u);
+        const uint32_t prow = ptx::mapa(sbase + C::kOffP + static_cast<uint32_t>(ps) * kPSlotBytes + h * 128u, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          ptx::st_async_v4(prow + (((4 * grp + j) ^ (h & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                           pk[4 * j + 3], pfull);
+        if (grp == 0)
+          ptx::st_async_b32(ptx::mapa(sbase + kOffAlpha + ps * 512u + h * 4u, 0), __float_as_uint(alpha), pfull);
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
+        if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
       if (!ok) break;
-      const bool split = slot_base[sg.b] >= 0;
-      const int slot = split ? group * spq + slot_base[sg.b] + (pl - first_pair[sg.b]) : -1;
-      const float lse_v = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -INFINITY;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      if (split) part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
-      else p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
-      if (!wait_warp<true>(BAR(MBEMPTY + ms), mphase ^ 1u, hdr)) { ok = false; break; }
-      const uint32_t mbfull = ptx::mapa(BAR(MBFULL + ms), 0);
-      ptx::mbar_arrive_expect_tx_remote(mbfull, 4u);
-      ptx::st_async_b32(ptx::mapa(sbase + kOffMail + ms * 512u + h * 4u, 0), __float_as_uint(inv_l), mbfull);
-      if (++ms == kMailSlots) { ms = 0; mphase ^= 1u; }
+      if (grp == 1) {
+        // hand group 1's partial sum to group 0 (read before group 0 loads the
+        // next segment's Q, so group 1 cannot overwrite it early)
+        l_part[h] = l;
+        ptx::mbar_arrive(BAR(LSUM));
+      } else {
+        if (!wait_warp<false>(BAR(LSUM), lsum_phase, hdr)) { ok = false; break; }
+        l += l_part[h];
+        const bool split = slot_base[sg.b] >= 0;
+        const int slot = split ? group * spq + slot_base[sg.b] + (pl - first_pair[sg.b]) : -1;
+        const float lse_v = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -INFINITY;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        if (split) part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
+        else p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
+        if (!wait_warp<true>(BAR(MBEMPTY + ms), mphase ^ 1u, hdr)) { ok = false; break; }
+        const uint32_t mbfull = ptx::mapa(BAR(MBFULL + ms), 0);
+        ptx::mbar_arrive_expect_tx_remote(mbfull, 4u);
+        ptx::st_async_b32(ptx::mapa(sbase + kOffMail + ms * 512u + h * 4u, 0), __float_as_uint(inv_l), mbfull);
+        if (++ms == kMailSlots) { ms = 0; mphase ^= 1u; }
+      }
+      lsum_phase ^= 1u;
     }
     // the last remote arrivals from rank 0 must land before this CTA exits
-    if (ok) {
+    if (ok && grp == 0) {
       for (int s = 0; s < kPSlots && ok; ++s) {
         ok = wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr);
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
@@ -826,8 +740,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   }
 }
 
-// Host-side launcher.  kMode 0: bf16 cache through the two tensor maps (K
-// boxes of 64 rows for rank 1, V boxes of 32 rows for rank 0); 1: FP8 cache
+// Host-side launcher.  kMode 0: bf16 cache through the two 3-D tensor maps
+// (whole-page boxes: nine chunks for rank 1, eight for rank 0); 1: FP8 cache
 // (p.kv_fp8; tensor maps unused).
 template <int kMode>
 cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
