@@ -408,11 +408,16 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             !wait_warp<false>(BAR(SEMPTY + sb), sphase ^ 1u, hdr)) { ok = false; break; }
         ptx::tc_fence_after();
         if (lane == 0) {
+          // descriptors built once per page; each of the 36 MMAs then costs an
+          // add and the issue (the start address is the descriptor's low field)
           const uint32_t d = tmem + kSCol + 64u * sb;
-#pragma unroll 4
+          const uint64_t lat0 = ptx::sdesc_sw128(sbase + C::k_chunk(stage, 0), 16, 1024);
+          const uint64_t rope0 = ptx::sdesc_sw128(sbase + C::k_chunk(stage, 8), 16, 1024);
+#pragma unroll
           for (int k = 0; k < kRow / 16; ++k) {
-            const uint32_t baddr = sbase + C::k_chunk(stage, k >> 2) + (k & 3) * 32;
-            const uint64_t bdesc = ptx::sdesc_sw128(baddr, 16, 1024);
+            const int c = k >> 2, kk = k & 3;
+            const uint64_t bdesc = c < 8 ? lat0 + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4)
+                                         : rope0 + static_cast<uint64_t>((kk * 32) >> 4);
             ptx::mma_ts(d, tmem + kQCol + 8u * k, bdesc, kIdescS, k > 0 ? 1u : 0u);
           }
           ptx::mma_commit(BAR(EMPTY + stage));
