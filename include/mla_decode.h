@@ -86,6 +86,41 @@ int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,
                     float softmax_scale, uint16_t* out, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* mla_decode_bf16 without a caller workspace.  The method has no
+ * counterpart to this call: it exists for callers that cannot hand the
+ * library device memory, such as a host that has already given (almost) all
+ * of HBM to its KV-cache pool, a loop that must not block in
+ * cudaMalloc/cudaFree (both may synchronise the device), or a foreign runtime
+ * that gives its plug-ins no device allocator.  The call itself allocates
+ * nothing: its scratch is one 40 MiB array that the library owns as a static
+ * device variable (one copy per device).
+ *
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's address (cudaGetSymbolAddress) and caches it; make that first
+ * call before any stream capture begins.  A failed look-up returns
+ * MLA_ERR_CUDA and is retried by the next call.
+ *
+ * Limit: batch * sq <= 8192 query rows, and a device with at most 76
+ * resident CTA pairs (152 SMs).  Larger requests return MLA_ERR_WORKSPACE
+ * before anything is queued.
+ *
+ * Concurrency: every call on one device shares the one scratch array.  Calls
+ * queued on the same stream are ordered and safe; calls whose work can
+ * overlap in time (other streams, other host threads) race on it and give
+ * undefined results.
+ *
+ * device_status: NULL, or 4 bytes of device memory, which receive this
+ * call's device status (MLA_OK or an MLA_STATUS_* code, as mla_get_status
+ * would report it) once the call's work has run on `stream`.  The status
+ * word is cleared at the start of every call.
+ * All other arguments, layouts and results are those of mla_decode_bf16. */
+int mla_decode_bf16_noalloc(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                            const uint16_t* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, int batch, int sq,
+                            int num_heads, int num_pages, int page_size,
+                            int max_pages, float softmax_scale, uint16_t* out,
+                            float* lse, int* device_status, void* stream);
+
 /* Same over the FP8 cache: each 594-byte row is dequantised as
  * v[k] = e4m3(byte[k]) * 2^(byte[576 + k/32] - 127) ("DeepSeek-R1" model
  * record, engine kernel constraint (2): e4m3 values, one e8m0 scale per 32)

@@ -27,6 +27,8 @@ SIGNATURES = {
     "mla_workspace_size": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_decode_bf16": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                              ctypes.c_size_t, _P]),
+    "mla_decode_bf16_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                                     _P]),
     "mla_decode_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                             ctypes.c_size_t, _P]),
     "mla_combine_splits": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
@@ -146,6 +148,40 @@ def mla_decode_bf16(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, 
     """MLA decode over a bf16 latent cache [num_pages, 64, 576]; returns (out, lse)."""
     return _decode("mla_decode_bf16", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
                    workspace, stream, torch.bfloat16, 576)
+
+
+def mla_decode_bf16_noalloc(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out=None, lse=None,
+                            device_status=None, stream=None):
+    """mla_decode_bf16 on the library's own static scratch (no workspace
+    argument; the library allocates nothing).  At most 8192 query rows;
+    calls that can overlap in time race on the shared scratch.
+    `device_status`: optional int32 CUDA tensor of one element that receives
+    the call's device status.  Returns (out, lse)."""
+    B, Sq, H, D = q_absorbed.shape
+    _check(q_absorbed, "q_absorbed", torch.bfloat16, (B, Sq, H, 512))
+    _check(q_rope, "q_rope", torch.bfloat16, (B, Sq, H, 64))
+    _check(kv_cache, "kv_cache", torch.bfloat16)
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != 576:
+        raise ValueError(f"kv_cache must be [num_pages, page_size, 576], got {tuple(kv_cache.shape)}")
+    _check(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Sq, H, 512), dtype=torch.bfloat16, device=q_absorbed.device)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=q_absorbed.device)
+    _check(out, "out", torch.bfloat16, (B, Sq, H, 512))
+    _check(lse, "lse", torch.float32, (B, Sq, H))
+    if device_status is not None:
+        _check(device_status, "device_status", torch.int32, (1,))
+    rc = load().mla_decode_bf16_noalloc(
+        _ptr(q_absorbed), _ptr(q_rope), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+        int(B), int(Sq), int(H), int(kv_cache.shape[0]), int(kv_cache.shape[1]), int(block_table.shape[1]),
+        ctypes.c_float(float(scale)), _ptr(out), _ptr(lse), _ptr(device_status), _stream(stream))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_bf16_noalloc")
+    return out, lse
 
 
 def mla_decode_fp8(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out=None, lse=None,

@@ -8,6 +8,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "decode.cuh"
 
@@ -115,6 +116,39 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   return MLA_OK;
 }
 
+// Library-owned scratch of mla_decode_bf16_noalloc: the plan header, the
+// split-KV plan and the fp32 partial outputs, for callers that cannot hand
+// the library device memory.  40 MiB holds the partials of 76 CTA pairs (the
+// 152 SMs of a GB300: 152 slots x 128 heads x 512 x 4 B = 38 MiB) plus the
+// plan of up to kStaticMaxRows query rows.  One copy per device, shared by
+// every call on that device.
+constexpr size_t kStaticScratchBytes = size_t{40} << 20;
+constexpr int kStaticMaxRows = 8192;
+constexpr int kStaticMaxDevices = 64;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kStaticMaxDevices] = {};
+
+// Device address of this device's copy of the scratch, looked up once per
+// device (with that device current) and cached.
+int static_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (dev < 0 || dev >= kStaticMaxDevices) return MLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -135,6 +169,33 @@ int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope, const ui
                     void* workspace, size_t workspace_bytes, void* stream) {
   return run_decode(false, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
                     page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_bf16_noalloc(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint16_t* kv_cache,
+                            const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
+                            int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out,
+                            float* lse, int* device_status, void* stream) {
+  void* scratch = nullptr;
+  int st = static_scratch(&scratch);
+  if (st != MLA_OK) return st;
+  st = validate_common(q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+                       page_size, max_pages, softmax_scale, out, lse, scratch);
+  if (st != MLA_OK) return st;
+  if (device_status && !aligned(device_status, 4)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(batch) * sq > kStaticMaxRows) return MLA_ERR_WORKSPACE;
+  const int pairs = decode_max_pairs();
+  if (pairs <= 0) return MLA_ERR_CUDA;
+  if (ws_layout(batch, sq, pairs).total > kStaticScratchBytes) return MLA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the status word and the abort flag must start at zero for this call
+  if (cudaMemsetAsync(scratch, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
+  st = run_decode(false, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+                  page_size, max_pages, softmax_scale, out, lse, scratch, kStaticScratchBytes, stream);
+  if (st != MLA_OK) return st;
+  if (device_status &&
+      cudaMemcpyAsync(device_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint8_t* kv_cache,
