@@ -33,18 +33,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The bf16 cache viewed as a 3-D tensor: (64 columns, num_pages*64 rows, 9
-// column chunks) with row stride 1152 B and chunk stride 128 B.  A box of
-// 64 x 64 x `chunks` is one whole page, written to shared memory chunk-major
-// (chunk c at c*8 KiB, 128-byte rows, 128B swizzle) in a single copy.
+// The bf16 cache viewed as a 4-D tensor: (64 columns, 8 rows, 9 column
+// chunks, num_pages*8 row groups) with strides 1152 B (row), 128 B (chunk)
+// and 9216 B (row group).  A box of 64 x 8 x `chunks` x 4 is one half page
+// (32 tokens), written to shared memory as 8-row x 128-byte swizzle atoms in
+// (row group, chunk, row) order, so consecutive half-page slots form one
+// K-major operand with a constant row-group stride.
 int make_cache_tmap(CUtensorMap* m, const void* cache, int num_pages, unsigned chunks) {
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_pages) * kPage, static_cast<cuuint64_t>(kRow / 64)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRow) * 2, 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kPage), chunks};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
+  cuuint64_t dims[4] = {64, 8, static_cast<cuuint64_t>(kRow / 64), static_cast<cuuint64_t>(num_pages) * (kPage / 8)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kRow) * 2, 128, static_cast<cuuint64_t>(kRow) * 2 * 8};
+  cuuint32_t box[4] = {64, 8, chunks, 4};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
@@ -83,7 +85,7 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   const WsLayout L = ws_layout(batch, sq, pairs);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  CUtensorMap tmap_k, tmap_v;    // whole pages: 9 chunks (score SM), 8 latent chunks (value SM)
+  CUtensorMap tmap_k, tmap_v;    // half pages: 9 chunks (score SM), 8 latent chunks (value SM)
   if (!fp8) {
     st = make_cache_tmap(&tmap_k, kv_cache, num_pages, 9);
     if (st == MLA_OK) st = make_cache_tmap(&tmap_v, kv_cache, num_pages, 8);

@@ -11,32 +11,38 @@
 // it.  Each 2-CTA cluster splits the work by role, not by data, and no FLOP
 // is computed twice:
 //   rank 1 ("score SM"): Q [128 x 576] bf16 resident in TMEM (288 columns);
-//       per 64-token page S = Q . K^T (36 tcgen05.mma, M=128, N=64, A from
-//       TMEM) into one of two 64-column S buffers; eight softmax warps in two
-//       groups (columns 0..31 and 32..63 of each head row; both take the row
-//       max over all 64 columns, so their reference maxima agree without an
+//       per tile of N tokens S = Q . K^T (36 tcgen05.mma, M=128, A from TMEM)
+//       into one of two N-column S buffers; eight softmax warps in two groups
+//       (each turns half of the tile's columns into P, both take the row max
+//       over all N columns, so their reference maxima agree without an
 //       exchange) round P to bf16 and send it with st.async into rank 0's
 //       shared memory in the 128B-swizzled K-major layout its MMA reads; the
 //       bytes are counted on rank 0's barrier, so no thread waits for them.
 //   rank 0 ("value SM"): O [128 x 512] fp32 in all 512 TMEM columns;
-//       O += P . V with P from shared memory and V read from the page tile as
-//       an MN-major operand (two M=128, N=256, K=16 MMAs per 16 tokens); its
-//       epilogue warps rescale O when rank 1 moves a head's reference max and
-//       write out = O / l (or an fp32 split partial).
-// Page loads.  One TMA operation per page per rank: the bf16 cache is
-// described as a 3-D tensor (64 columns, rows, 9 column chunks) with row
-// stride 1152 B and chunk stride 128 B, so a single box of 64 x 64 x 9 (rank
-// 1, 72 KiB) or 64 x 64 x 8 (rank 0, 64 KiB) lands as nine (eight) 128B-
-// swizzled chunks of 64 rows -- exactly the operand layout -- in one copy.
-// An SM's copy engine streams far more bytes per second in large operations
-// than in 8 KiB boxes, so whole-page copies are what lets 152 SMs reach HBM
-// speed.  Both ranks read every page; the second read is an L2 hit.  The FP8
-// cache is bulk-copied as raw half pages and dequantised by four warps into
-// the same layouts.
+//       O += P . V with P from shared memory and V read as an MN-major operand
+//       (two M=128, N=256, K=16 MMAs per 16 tokens); its epilogue warps
+//       rescale O when rank 1 moves a head's reference max and write
+//       out = O / l (or an fp32 split partial).
+//
+// Tiles of 96 tokens.  A tcgen05.mma with N <= 96 costs about as much as one
+// with N = 64, so the score SM works on 96-token tiles (three half pages).
+// The cache is described to TMA as a 4-D tensor (64 columns, 8 rows, 9
+// column chunks, 8-row groups) with strides 1152 B (row), 128 B (chunk) and
+// 9216 B (row group); one box of 4 row groups is a half page (32 tokens,
+// 36 KiB with all nine chunks, 32 KiB with the eight latent chunks) and
+// lands as 8-row x 128-byte swizzle atoms ordered (row group, chunk, row).
+// Consecutive half-page slots therefore continue each other's row-group
+// sequence at a constant 9216-byte stride, so three adjacent slots are one
+// 96-row K-major operand, whatever pages they came from.  The value SM keeps
+// half-page V slots (atoms at 1 KiB per chunk, 8 KiB per row group), read as
+// MN-major operands 16 tokens at a time.  Both ranks read every half page;
+// the second read is an L2 hit.  The FP8 cache is bulk-copied as raw half
+// pages and dequantised by four warps into the same layouts (64-token tiles
+// there, as the raw buffers take the shared memory of the third slot).
 //
 // Lazy rescaling: rank 1 keeps a per-head reference max m_ref (raw score
-// units) and moves it only when a page's max exceeds it by more than 8 in
-// log2 units, so P <= 256 and O is rescaled only on those rare pages.
+// units) and moves it only when a tile's max exceeds it by more than 8 in
+// log2 units, so P <= 256 and O is rescaled only on those rare tiles.
 //
 // Every wait is bounded (wait_bounded / wait_warp); a timeout records
 // MLA_STATUS_TIMEOUT and raises an abort flag so every role leaves its loop
@@ -53,47 +59,50 @@ namespace mla {
 
 namespace dk {
 
-constexpr uint32_t kChunkBytes = 64 * 128;            // 64 rows x 64 bf16, 128B swizzle
-constexpr uint32_t kVPageBytes = 8 * kChunkBytes;     // latent c_KV part of one page (64 KiB)
-constexpr uint32_t kPSlotBytes = 128 * 128;           // P of one page: 128 heads x 64 tokens bf16
+constexpr uint32_t kAtom = 1024;                        // 8 rows x 128 B, 128B swizzle
+constexpr uint32_t kKSlot = 4 * 9 * kAtom;             // half page, nine chunks (36 KiB)
+constexpr uint32_t kKGroup = 9 * kAtom;                // row-group stride of a K slot
+constexpr uint32_t kVSlot = 4 * 8 * kAtom;             // half page, eight latent chunks (32 KiB)
+constexpr uint32_t kVGroup = 8 * kAtom;                // row-group stride of a V slot
+constexpr uint32_t kPChunk = 128 * 128;                // 64 tokens of P for 128 heads (16 KiB)
 constexpr int kPSlots = 2;
 constexpr int kMailSlots = 2;
-constexpr uint32_t kRawBytes = 32 * kFp8Row;          // half a page of FP8 rows: 19,008 B
-constexpr int kMaxStages = 3, kMaxRaw = 4;
+constexpr int kHalf = kPage / 2;                        // tokens per half page
+constexpr uint32_t kRawBytes = kHalf * kFp8Row;         // raw FP8 half page: 19,008 B
+constexpr int kMaxVSlots = 5, kMaxRaw = 4;
 
 // Shared-memory plans (bytes).  The small common region (alpha, 1/l, flags,
 // barriers) sits at the same offset in both ranks so remote stores and
 // arrivals can address it.
-//   bf16: rank 1 = 3 K pages of 72 KiB (chunks 0..8 contiguous);
-//         rank 0 = 3 V pages of 64 KiB + 2 P slots.
-//   FP8:  rank 1 = 2 bf16 K pages (latent chunks at stage*64K, RoPE chunk in
-//         a separate ring) + 4 raw half pages; rank 0 = 2 V pages + 2 P slots
-//         + 3 raw half pages.
+//   bf16: rank 1 = 6 K slots (two 3-slot tiles); rank 0 = 5 V slots + 2 P
+//         slots of two chunks (96 tokens).
+//   FP8:  rank 1 = 4 K slots (two 2-slot tiles) + 4 raw half pages; rank 0 =
+//         3 V slots + 2 one-chunk P slots + 3 raw half pages.
 template <int kMode> struct Cfg;
 template <> struct Cfg<0> {
-  static constexpr int kStages = 3;
+  static constexpr int kTileHalves = 3;
+  static constexpr int kVSlots = 5;
   static constexpr int kRaw1 = 0, kRaw0 = 0;
-  static constexpr uint32_t kKStageBytes = 9 * kChunkBytes;
-  static constexpr uint32_t kOffRope = 0;                           // unused: RoPE chunk is chunk 8 of the stage
-  static constexpr uint32_t kOffP = kStages * kVPageBytes;
+  static constexpr uint32_t kPSlotBytes = 2 * kPChunk;
+  static constexpr uint32_t kOffP = kVSlots * kVSlot;
   static constexpr uint32_t kOffRaw1 = 0, kOffRaw0 = 0;
-  static constexpr uint32_t kOffMisc = kOffP + kPSlots * kPSlotBytes;
+  static constexpr uint32_t kEnd1 = 2 * kTileHalves * kKSlot;
+  static constexpr uint32_t kEnd0 = kOffP + kPSlots * kPSlotBytes;
+  static constexpr uint32_t kOffMisc = kEnd1 > kEnd0 ? kEnd1 : kEnd0;
   static constexpr int kThreads = 384;
-  __device__ static uint32_t k_chunk(int stage, int c) { return stage * kKStageBytes + c * kChunkBytes; }
 };
 template <> struct Cfg<1> {
-  static constexpr int kStages = 2;
+  static constexpr int kTileHalves = 2;
+  static constexpr int kVSlots = 3;
   static constexpr int kRaw1 = 4, kRaw0 = 3;
-  static constexpr uint32_t kKStageBytes = kVPageBytes;
-  static constexpr uint32_t kOffRope = kStages * kVPageBytes;       // rank 1: RoPE chunk ring
-  static constexpr uint32_t kOffP = kStages * kVPageBytes;          // rank 0: P slots
-  static constexpr uint32_t kOffRaw1 = kOffRope + kStages * kChunkBytes;
+  static constexpr uint32_t kPSlotBytes = kPChunk;
+  static constexpr uint32_t kOffP = kVSlots * kVSlot;
+  static constexpr uint32_t kOffRaw1 = 2 * kTileHalves * kKSlot;
   static constexpr uint32_t kOffRaw0 = kOffP + kPSlots * kPSlotBytes;
-  static constexpr uint32_t kOffMisc = kOffRaw1 + kRaw1 * kRawBytes;
+  static constexpr uint32_t kEnd1 = kOffRaw1 + kRaw1 * kRawBytes;
+  static constexpr uint32_t kEnd0 = kOffRaw0 + kRaw0 * kRawBytes;
+  static constexpr uint32_t kOffMisc = ((kEnd1 > kEnd0 ? kEnd1 : kEnd0) + 127) & ~127u;
   static constexpr int kThreads = 512;
-  __device__ static uint32_t k_chunk(int stage, int c) {
-    return c < 8 ? stage * kVPageBytes + c * kChunkBytes : kOffRope + stage * kChunkBytes;
-  }
 };
 constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
 constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
@@ -102,8 +111,9 @@ constexpr uint32_t kMiscReq = 2048;      // rank 0: P slot of a rescale request
 constexpr uint32_t kMiscRawFlag = 2064;  // per raw stage: 1 = write zeros (bad page)
 constexpr uint32_t kMiscBar = 2080;
 enum Bar {
-  FULL = 0, EMPTY = FULL + kMaxStages,
-  PFULL = EMPTY + kMaxStages, PEMPTY = PFULL + kPSlots,
+  KFULL = 0, KEMPTY = KFULL + 2,
+  VFULL = KEMPTY + 2, VEMPTY = VFULL + kMaxVSlots,
+  PFULL = VEMPTY + kMaxVSlots, PEMPTY = PFULL + kPSlots,
   SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + 2,
   QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY, LSUM,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
@@ -114,15 +124,15 @@ constexpr uint32_t kMiscTmem = kMiscBar + NBAR * 8;
 constexpr uint32_t kMiscBytes = kMiscTmem + 16;
 template <int kMode> constexpr uint32_t smem_bytes() { return Cfg<kMode>::kOffMisc + kMiscBytes; }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory budget");
-static_assert(3 * 9 * kChunkBytes <= Cfg<0>::kOffMisc, "rank 1 plan (bf16)");
-static_assert(Cfg<1>::kOffRaw0 + Cfg<1>::kRaw0 * kRawBytes <= Cfg<1>::kOffMisc, "rank 0 plan (fp8)");
+static_assert(Cfg<0>::kVSlots <= kMaxVSlots && Cfg<1>::kVSlots <= kMaxVSlots, "V slot barriers");
+static_assert(Cfg<1>::kRaw1 <= kMaxRaw && Cfg<1>::kRaw0 <= kMaxRaw, "raw barriers");
+static_assert(Cfg<0>::kOffMisc % 1024 == 0, "slot alignment");
 
 // TMEM columns.
 constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
-constexpr uint32_t kSCol = 320;    // rank 1: two S buffers of 64 columns
+constexpr uint32_t kSCol = 320;    // rank 1: two S buffers of N columns (N <= 96)
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescS = ptx::idesc_bf16(128, 64, 0, 0);    // A = Q (TMEM, K-major), B = K (K-major)
 constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 256, 0, 1);  // A = P (K-major), B = V (MN-major)
 
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -134,7 +144,8 @@ struct Segment {
 };
 
 // Walks the segments of one pair: the pair's page range [lo, hi) cut at row
-// boundaries.  Every role of both ranks walks the same sequence.
+// boundaries.  Every role of both ranks walks the same sequence; inside a
+// segment the half pages [2*t0, 2*t1) are taken kTileHalves at a time.
 struct SegWalker {
   const int* tile_start;
   int batch, b, lo, hi;
@@ -211,10 +222,12 @@ __device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint32_
   dequant32(wd, row[kRow + g], o);
 }
 
-// Store 16 bf16x2 words (32 values of value group g) into row `r` of a
-// 128B-swizzled chunk whose 128-byte rows hold 64 values (two groups).
-__device__ __forceinline__ void store_group(uint8_t* chunk, int r, int g, const uint32_t* o) {
-  uint8_t* dst = chunk + r * 128;
+// Store 16 bf16x2 words (32 values of value group g) as token r of a
+// half-page slot whose 8-row atoms are `group_stride` bytes apart per row
+// group (chunk c = g/2 at c KiB inside the group, 128-byte rows, 128B
+// swizzle: 16-byte piece j of row r sits at piece j ^ (r % 8)).
+__device__ __forceinline__ void store_group(uint8_t* slot, uint32_t group_stride, int r, int g, const uint32_t* o) {
+  uint8_t* dst = slot + (r >> 3) * group_stride + (g >> 1) * kAtom + (r & 7) * 128;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int piece = ((g & 1) * 4 + j) ^ (r & 7);
@@ -230,7 +243,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                        const DecodeParams p) {
   using namespace dk;
   using C = Cfg<kMode>;
-  constexpr int kStages = C::kStages;
+  constexpr int TH = C::kTileHalves;            // half pages per tile
+  constexpr int kN = TH * kHalf;                // tokens per tile (S columns)
+  constexpr int kHC = kN / 2;                   // S columns per softmax group
+  constexpr int kVSlots = C::kVSlots;
+  constexpr uint32_t kIdescS = ptx::idesc_bf16(128, kN, 0, 0);   // A = Q (TMEM), B = K (K-major)
   constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
   constexpr uint32_t kOffMail = C::kOffMisc + kMiscMail;
   constexpr uint32_t kOffReq = C::kOffMisc + kMiscReq;
@@ -251,13 +268,20 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   float* part_lse = reinterpret_cast<float*>(p.ws + p.L.part_lse);
   float* part_out = reinterpret_cast<float*>(p.ws + p.L.part_out);
   auto BAR = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+  // physical page of row-local half page hp of batch row b (or -1 if out of range)
+  auto half_page = [&](int b, int hp) -> int {
+    const int page = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + (hp >> 1));
+    return (page < 0 || page >= p.num_pages) ? -1 : page;
+  };
 
   const bool smem_ok = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
     if (!smem_ok) set_status(&hdr->status, MLA_ERR_UNSUPPORTED);
-    for (int s = 0; s < kMaxStages; ++s) {
-      ptx::mbar_init(BAR(FULL + s), kMode == 0 ? 1u : 4u);   // TMA bytes, or the 4 dequant warps
-      ptx::mbar_init(BAR(EMPTY + s), 1);
+    // K tiles: the TMA bytes (bf16) or the four dequant warps (FP8)
+    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : 4u); ptx::mbar_init(BAR(KEMPTY + s), 1); }
+    for (int s = 0; s < kMaxVSlots; ++s) {
+      ptx::mbar_init(BAR(VFULL + s), kMode == 0 ? 1u : 4u);
+      ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 256); ptx::mbar_init(BAR(PEMPTY + s), 1); }
     for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 256); }
@@ -298,42 +322,54 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       const uint64_t pol = ptx::policy_evict_normal();
       SegWalker w; w.init(tile_start, p.batch, lo, hi);
       Segment sg;
-      int stage = 0; uint32_t phase = 0;
-      int rs = 0; uint32_t rphase = 0;
+      int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
+      int vs = 0; uint32_t vphase = 0;      // rank 0: V slot
+      int rs = 0; uint32_t rphase = 0;      // FP8: raw ring
       const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
       const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
       volatile uint32_t* raw_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffRawFlag);
       bool ok = true;
       while (ok && w.next(sg)) {
-        for (int t = sg.t0; t < sg.t1 && ok; ++t) {
-          int page = __ldg(p.block_table + static_cast<size_t>(sg.b) * p.max_pages + t);
-          const bool bad = page < 0 || page >= p.num_pages;
-          if (bad) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
+        const int hp_end = 2 * sg.t1;
+        for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
+          const int nh = min(TH, hp_end - h0);
           if constexpr (kMode == 0) {
-            // one copy per page: rank 1 all nine chunks (72 KiB), rank 0 the
-            // eight latent chunks (64 KiB); a bad page is read fully outside
-            // the tensor, which fills zeros
-            if (!wait_bounded<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
-            const int y = (bad ? p.num_pages : page) * kPage;
+            // a bad page is read fully outside the tensor, which fills zeros
             if (rank == 1) {
-              ptx::mbar_arrive_expect_tx(BAR(FULL + stage), 9u * kChunkBytes);
-              ptx::tma_load_3d(sbase + C::k_chunk(stage, 0), &tmap_k, BAR(FULL + stage), 0, y, 0, pol);
+              if (!wait_bounded<true>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+              ptx::mbar_arrive_expect_tx(BAR(KFULL + kb), static_cast<uint32_t>(nh) * kKSlot);
+              for (int j = 0; j < nh; ++j) {
+                const int hp = h0 + j, page = half_page(sg.b, hp);
+                if (page < 0) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
+                const int wq = (page < 0 ? p.num_pages : page) * 8 + (hp & 1) * 4;
+                ptx::tma_load_4d(sbase + static_cast<uint32_t>(kb * TH + j) * kKSlot, &tmap_k, BAR(KFULL + kb),
+                                 0, 0, 0, wq, pol);
+              }
+              kb ^= 1;
+              if (kb == 0) kphase ^= 1u;
             } else {
-              ptx::mbar_arrive_expect_tx(BAR(FULL + stage), kVPageBytes);
-              ptx::tma_load_3d(sbase + static_cast<uint32_t>(stage) * kVPageBytes, &tmap_v, BAR(FULL + stage),
-                               0, y, 0, pol);
+              for (int j = 0; j < nh; ++j) {
+                if (!wait_bounded<true>(BAR(VEMPTY + vs), vphase ^ 1u, hdr)) { ok = false; break; }
+                const int hp = h0 + j, page = half_page(sg.b, hp);
+                const int wq = (page < 0 ? p.num_pages : page) * 8 + (hp & 1) * 4;
+                ptx::mbar_arrive_expect_tx(BAR(VFULL + vs), kVSlot);
+                ptx::tma_load_4d(sbase + static_cast<uint32_t>(vs) * kVSlot, &tmap_v, BAR(VFULL + vs), 0, 0, 0, wq,
+                                 pol);
+                if (++vs == kVSlots) { vs = 0; vphase ^= 1u; }
+              }
             }
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
           } else {
-            // two raw half pages; a bad page is never read (dequant writes zeros)
-            for (int half = 0; half < 2; ++half) {
+            // raw half pages; a bad page is never read (dequant writes zeros)
+            for (int j = 0; j < nh; ++j) {
               if (!wait_bounded<true>(BAR(RAWEMPTY + rs), rphase ^ 1u, hdr)) { ok = false; break; }
-              raw_flag[rs] = bad ? 1u : 0u;
-              if (bad) {
+              const int hp = h0 + j, page = half_page(sg.b, hp);
+              if (page < 0 && rank == 1) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
+              raw_flag[rs] = page < 0 ? 1u : 0u;
+              if (page < 0) {
                 ptx::mbar_arrive(BAR(RAWFULL + rs));
               } else {
                 ptx::mbar_arrive_expect_tx(BAR(RAWFULL + rs), kRawBytes);
-                const uint8_t* src = p.kv_fp8 + static_cast<size_t>(page) * (kPage * kFp8Row) + half * kRawBytes;
+                const uint8_t* src = p.kv_fp8 + static_cast<size_t>(page) * (kPage * kFp8Row) + (hp & 1) * kRawBytes;
                 ptx::bulk_load(sbase + raw_off + static_cast<uint32_t>(rs) * kRawBytes, src, kRawBytes,
                                BAR(RAWFULL + rs), pol);
               }
@@ -345,10 +381,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     }
   } else if (kMode == 1 && active && warp >= 12) {
     // ------------------------------------------------------------ FP8 dequant (warps 12..15)
-    // raw half page -> bf16 operand rows [32*half, 32*half+32) of the page.
-    // Warp wq handles tokens of parity (wq & 1) (so the row's 2-byte
-    // misalignment is warp-uniform) and half of the 32-value groups (9 of 18
-    // on rank 1, 8 of the 16 latent groups on rank 0).
+    // raw half page -> one bf16 slot (32 tokens).  Warp wq handles tokens of
+    // parity (wq & 1) (so the row's 2-byte misalignment is warp-uniform) and
+    // half of the 32-value groups (9 of 18 on rank 1, 8 of the 16 latent
+    // groups on rank 0).
     const int wq = warp - 12;
     const int parity = wq & 1;
     const int G = rank == 1 ? 9 : 8;
@@ -356,16 +392,27 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     const int n_tasks = 16 * G;
     const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
     const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
+    const uint32_t gstride = rank == 1 ? kKGroup : kVGroup;
     const volatile uint32_t* raw_flag = reinterpret_cast<const volatile uint32_t*>(smem + kOffRawFlag);
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int stage = 0; uint32_t phase = 0;
+    int kb = 0; uint32_t kphase = 0;
+    int vs = 0; uint32_t vphase = 0;
     int rs = 0; uint32_t rphase = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
-      for (int t = sg.t0; t < sg.t1 && ok; ++t) {
-        if (!wait_warp<true>(BAR(EMPTY + stage), phase ^ 1u, hdr)) { ok = false; break; }
-        for (int half = 0; half < 2; ++half) {
+      const int hp_end = 2 * sg.t1;
+      for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
+        const int nh = min(TH, hp_end - h0);
+        if (rank == 1 && !wait_warp<true>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+        for (int j = 0; j < nh; ++j) {
+          uint8_t* slot;
+          if (rank == 1) {
+            slot = smem + static_cast<uint32_t>(kb * TH + j) * kKSlot;
+          } else {
+            if (!wait_warp<true>(BAR(VEMPTY + vs), vphase ^ 1u, hdr)) { ok = false; break; }
+            slot = smem + static_cast<uint32_t>(vs) * kVSlot;
+          }
           if (!wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
           const bool zero = raw_flag[rs] != 0;
           const uint8_t* raw = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes;
@@ -379,60 +426,69 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
 #pragma unroll
               for (int i = 0; i < 16; ++i) o[i] = 0u;
             }
-            store_group(smem + C::k_chunk(stage, g >> 1), 32 * half + tok, g, o);
+            store_group(slot, gstride, tok, g, o);
           }
           ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA (async proxy)
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(BAR(RAWEMPTY + rs));
+          if (lane == 0) {
+            ptx::mbar_arrive(BAR(RAWEMPTY + rs));
+            if (rank == 0) ptx::mbar_arrive(BAR(VFULL + vs));
+          }
           if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
+          if (rank == 0 && ++vs == kVSlots) { vs = 0; vphase ^= 1u; }
         }
         if (!ok) break;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(BAR(FULL + stage));
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (rank == 1) {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(BAR(KFULL + kb));
+          kb ^= 1;
+          if (kb == 0) kphase ^= 1u;
+        }
       }
     }
   } else if (active && warp == 1 && rank == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
+    // One tile = TH adjacent half-page slots = one kN-row K-major operand
+    // (8-row atoms every kKGroup bytes); K-step k reads chunk k/4 at byte
+    // 32*(k%4) inside the atoms.
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int stage = 0; uint32_t phase = 0;
+    int kb = 0; uint32_t kphase = 0;
     int sb = 0; uint32_t sphase = 0;
     uint32_t qphase = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
       if (!wait_warp<false>(BAR(QREADY), qphase, hdr)) break;
       qphase ^= 1u;
-      for (int t = sg.t0; t < sg.t1 && ok; ++t) {
-        if (!wait_warp<false>(BAR(FULL + stage), phase, hdr) ||
+      const int hp_end = 2 * sg.t1;
+      for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
+        if (!wait_warp<false>(BAR(KFULL + kb), kphase, hdr) ||
             !wait_warp<false>(BAR(SEMPTY + sb), sphase ^ 1u, hdr)) { ok = false; break; }
         ptx::tc_fence_after();
         if (lane == 0) {
-          // descriptors built once per page; each of the 36 MMAs then costs an
-          // add and the issue (the start address is the descriptor's low field)
-          const uint32_t d = tmem + kSCol + 64u * sb;
-          const uint64_t lat0 = ptx::sdesc_sw128(sbase + C::k_chunk(stage, 0), 16, 1024);
-          const uint64_t rope0 = ptx::sdesc_sw128(sbase + C::k_chunk(stage, 8), 16, 1024);
+          const uint32_t d = tmem + kSCol + static_cast<uint32_t>(kN * sb);
+          const uint64_t desc0 = ptx::sdesc_sw128(sbase + static_cast<uint32_t>(kb * TH) * kKSlot, 16, kKGroup);
 #pragma unroll
           for (int k = 0; k < kRow / 16; ++k) {
-            const int c = k >> 2, kk = k & 3;
-            const uint64_t bdesc = c < 8 ? lat0 + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4)
-                                         : rope0 + static_cast<uint64_t>((kk * 32) >> 4);
+            const uint64_t bdesc = desc0 + static_cast<uint64_t>(((k >> 2) * kAtom + (k & 3) * 32) >> 4);
             ptx::mma_ts(d, tmem + kQCol + 8u * k, bdesc, kIdescS, k > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(BAR(EMPTY + stage));
+          ptx::mma_commit(BAR(KEMPTY + kb));
           ptx::mma_commit(BAR(SFULL + sb));
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        kb ^= 1;
+        if (kb == 0) kphase ^= 1u;
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
       }
     }
   } else if (active && warp == 1 && rank == 0) {
     // ------------------------------------------------------------ O += P V issuer
+    // Per half page of the tile: two K-steps of 16 tokens (two row groups of
+    // the V slot each), two N=256 halves of the latent columns per step.
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int stage = 0; uint32_t phase = 0;
+    int vs = 0; uint32_t vphase = 0;
     int ps = 0; uint32_t pphase = 0;
     uint32_t corr_phase = 0, oe_phase = 0;
     bool first_seg = true, ok = true;
@@ -440,11 +496,12 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     const volatile float* alpha_buf = reinterpret_cast<const volatile float*>(smem + kOffAlpha);
     while (ok && w.next(sg)) {
       const int len_i = lens[sg.b] - (sq - 1 - group);
-      for (int t = sg.t0; t < sg.t1 && ok; ++t) {
-        if (!wait_warp<false>(BAR(FULL + stage), phase, hdr) ||
-            !wait_warp<true>(BAR(PFULL + ps), pphase, hdr)) { ok = false; break; }
+      const int hp_end = 2 * sg.t1;
+      for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
+        const int nh = min(TH, hp_end - h0);
+        if (!wait_warp<true>(BAR(PFULL + ps), pphase, hdr)) { ok = false; break; }
         ptx::fence_proxy_async_cta();
-        // did rank 1 move its reference max for any head of this page?
+        // did rank 1 move its reference max for any head of this tile?
         bool moved = false;
 #pragma unroll
         for (int i = 0; i < 4; ++i) moved |= alpha_buf[ps * 128 + lane * 4 + i] != 1.f;
@@ -459,52 +516,61 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           if (!wait_warp<false>(BAR(CORR), corr_phase, hdr)) { ok = false; break; }
           corr_phase ^= 1u;
         }
-        if (t == sg.t0 && !first_seg) {
+        if (h0 == 2 * sg.t0 && !first_seg) {
           if (!wait_warp<false>(BAR(OEMPTY), oe_phase, hdr)) { ok = false; break; }
           oe_phase ^= 1u;
         }
-        const uint32_t vpage = static_cast<uint32_t>(stage) * kVPageBytes;
-        const int valid = len_i - t * kPage;   // rows of this page visible to the query
-        if (valid < kPage) {
-          // rows past the visible length get P = 0; make their V finite too
-          const int v0 = valid > 0 ? valid : 0;
-          uint4* base = reinterpret_cast<uint4*>(smem + vpage);
-          const int n16 = (kPage - v0) * 8;     // 16-byte pieces per chunk
-          for (int c = 0; c < 8; ++c)
-            for (int i = lane; i < n16; i += 32)
-              base[(c * kChunkBytes + v0 * 128) / 16 + i] = make_uint4(0, 0, 0, 0);
-          ptx::fence_proxy_async_cta();
-          __syncwarp();
-        }
-        ptx::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t pbase = sbase + C::kOffP + static_cast<uint32_t>(ps) * kPSlotBytes;
-          const uint32_t vbase = sbase + vpage;
-#pragma unroll
-          for (int k = 0; k < kPage / 16; ++k) {
-            const uint64_t adesc = ptx::sdesc_sw128(pbase + k * 32, 16, 1024);
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-              const uint64_t bdesc = ptx::sdesc_sw128(vbase + n * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024);
-              ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, (t > sg.t0 || k > 0) ? 1u : 0u);
+        const uint32_t pbase = sbase + C::kOffP + static_cast<uint32_t>(ps) * C::kPSlotBytes;
+        for (int j = 0; j < nh; ++j) {
+          if (!wait_warp<false>(BAR(VFULL + vs), vphase, hdr)) { ok = false; break; }
+          const int valid = len_i - (h0 + j) * kHalf;   // tokens of this half page visible to the query
+          if (valid < kHalf) {
+            // rows past the visible length get P = 0; make their V finite too
+            const int v0 = valid > 0 ? valid : 0;
+            uint8_t* slot = smem + static_cast<uint32_t>(vs) * kVSlot;
+            for (int i = lane; i < (kHalf - v0) * 8 * 8; i += 32) {   // rows x chunks x 16-byte pieces
+              const int r = v0 + i / 64, c = (i / 8) & 7, q = i & 7;
+              *reinterpret_cast<uint4*>(slot + (r >> 3) * kVGroup + c * kAtom + (r & 7) * 128 + q * 16) =
+                  make_uint4(0, 0, 0, 0);
             }
+            ptx::fence_proxy_async_cta();
+            __syncwarp();
           }
-          ptx::mma_commit(BAR(EMPTY + stage));
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t vbase = sbase + static_cast<uint32_t>(vs) * kVSlot;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              const int k = 2 * j + s;                   // K-step of the tile
+              const uint64_t adesc = ptx::sdesc_sw128(pbase + (k >> 2) * kPChunk + (k & 3) * 32, 16, 1024);
+#pragma unroll
+              for (int n = 0; n < 2; ++n) {
+                const uint64_t bdesc =
+                    ptx::sdesc_sw128(vbase + static_cast<uint32_t>(s * 2) * kVGroup + n * 4 * kAtom, kAtom, kVGroup);
+                ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, (h0 > 2 * sg.t0 || k > 0) ? 1u : 0u);
+              }
+            }
+            ptx::mma_commit(BAR(VEMPTY + vs));
+          }
+          __syncwarp();
+          if (++vs == kVSlots) { vs = 0; vphase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) {
           ptx::mma_commit_mc(BAR(PEMPTY + ps), static_cast<uint16_t>(1u << 1));
-          if (t == sg.t1 - 1) ptx::mma_commit(BAR(OFULL));
+          if (h0 + TH >= hp_end) ptx::mma_commit(BAR(OFULL));
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
       first_seg = false;
     }
   } else if (active && warp >= 4 && warp < 12 && rank == 1) {
     // ------------------------------------------------------------ softmax (thread = head)
-    // Group 0 (warps 4..7) turns columns 0..31 of each page's S into P, group
-    // 1 (warps 8..11) columns 32..63.  Both take the row max over all 64
-    // columns, so their reference maxima and rescale factors agree without an
-    // exchange; the two partial sums meet once per segment (LSUM barrier).
+    // Group 0 (warps 4..7) turns columns [0, kHC) of each tile's S into P,
+    // group 1 (warps 8..11) columns [kHC, kN).  Both take the row max over all
+    // kN columns, so their reference maxima and rescale factors agree without
+    // an exchange; the two partial sums meet once per segment (LSUM barrier).
     const int grp = (warp - 4) >> 2;
     const int h = (threadIdx.x - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -548,38 +614,45 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         ptx::mbar_arrive(BAR(QREADY));
       }
       float m_ref = -INFINITY, l = 0.f;
-      for (int t = sg.t0; t < sg.t1; ++t) {
+      const int hp_end = 2 * sg.t1;
+      for (int h0 = 2 * sg.t0; h0 < hp_end; h0 += TH) {
         if (!wait_warp<false>(BAR(SFULL + sb), sphase, hdr)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t sadr = tmem + lane_base + kSCol + 64u * sb;
-        uint32_t mine[32], other[32];
-        ptx::tmem_ld32(sadr + 32u * grp, mine);
-        ptx::tmem_ld32(sadr + 32u * (grp ^ 1), other);
+        const uint32_t sadr = tmem + lane_base + kSCol + static_cast<uint32_t>(kN * sb);
+        const int c_mine = kHC * grp, c_other = kHC * (grp ^ 1);
+        uint32_t mine[kHC], other[kHC];
+#pragma unroll
+        for (int j = 0; j < kHC / 16; ++j) {
+          ptx::tmem_ld16(sadr + c_mine + 16 * j, mine + 16 * j);
+          ptx::tmem_ld16(sadr + c_other + 16 * j, other + 16 * j);
+        }
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         ptx::mbar_arrive(BAR(SEMPTY + sb));
-        const int valid = len_i - t * kPage;          // columns of this page visible to the query
-        const int c_mine = 32 * grp, c_other = 32 * (grp ^ 1);
+        // columns of this tile visible to the query: within the row's length
+        // and within the half pages this tile loaded (the segment may end
+        // before the row does; slots past it hold stale data)
+        const int valid = min(len_i - h0 * kHalf, min(TH, hp_end - h0) * kHalf);
         // row max of the masked raw scores.  m_ref stays in raw score units and
         // P = exp2((s - m_ref) * c), so the max element gets exactly exp2(0) = 1
         // whatever the magnitude of the scores (scale c > 0).
         float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < kHC; ++e) {
           if (c_mine + e < valid) mx = fmaxf(mx, __uint_as_float(mine[e]));
           if (c_other + e < valid) mx = fmaxf(mx, __uint_as_float(other[e]));
         }
         float alpha = 1.f;
-        if (t == sg.t0) {
+        if (h0 == 2 * sg.t0) {
           m_ref = mx;
         } else if ((mx - m_ref) * c > kRescaleThreshold) {
           alpha = fast_exp2((m_ref - mx) * c);
           l *= alpha;
           m_ref = mx;
         }
-        uint32_t pk[16];
+        uint32_t pk[kHC / 2];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < kHC / 2; ++e) {
           const int col = c_mine + 2 * e;
           const float p0 = col < valid ? fast_exp2((__uint_as_float(mine[2 * e]) - m_ref) * c) : 0.f;
           const float p1 = col + 1 < valid ? fast_exp2((__uint_as_float(mine[2 * e + 1]) - m_ref) * c) : 0.f;
@@ -588,16 +661,19 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
         if (m_ref == -INFINITY) l = 0.f;     // nothing visible yet (every p was 0)
         if (!wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr)) { ok = false; break; }
-        // This group's half of P row h (64 B, swizzled) -- and, from group 0,
-        // alpha_h -- go to rank 0 as st.async bytes counted on its PFULL
-        // barrier: nobody waits for them here.
+        // This group's columns of P row h (kHC/8 pieces of 16 B: piece q holds
+        // tokens 8q..8q+7, in chunk q/8 at swizzled position (q%8) ^ (h%8)) --
+        // and, from group 0, alpha_h -- go to rank 0 as st.async bytes counted
+        // on its PFULL barrier: nobody waits for them here.
         const uint32_t pfull = ptx::mapa(BAR(PFULL + ps), 0);
-        ptx::mbar_arrive_expect_tx_remote(pfull, grp == 0 ? 4u * 16u + 4u : 4u * 16u);
-        const uint32_t prow = ptx::mapa(sbase + C::kOffP + static_cast<uint32_t>(ps) * kPSlotBytes + h * 128u, 0);
+        ptx::mbar_arrive_expect_tx_remote(pfull, grp == 0 ? 2u * kHC + 4u : 2u * kHC);
+        const uint32_t prow = ptx::mapa(sbase + C::kOffP + static_cast<uint32_t>(ps) * C::kPSlotBytes + h * 128u, 0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          ptx::st_async_v4(prow + (((4 * grp + j) ^ (h & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
-                           pk[4 * j + 3], pfull);
+        for (int j = 0; j < kHC / 8; ++j) {
+          const int q = grp * (kHC / 8) + j;
+          ptx::st_async_v4(prow + static_cast<uint32_t>(q >> 3) * kPChunk + ((static_cast<uint32_t>(q & 7) ^ (h & 7)) << 4),
+                           pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], pfull);
+        }
         if (grp == 0)
           ptx::st_async_b32(ptx::mapa(sbase + kOffAlpha + ps * 512u + h * 4u, 0), __float_as_uint(alpha), pfull);
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
@@ -745,8 +821,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   }
 }
 
-// Host-side launcher.  kMode 0: bf16 cache through the two 3-D tensor maps
-// (whole-page boxes: nine chunks for rank 1, eight for rank 0); 1: FP8 cache
+// Host-side launcher.  kMode 0: bf16 cache through the two 4-D tensor maps
+// (half-page boxes: nine chunks for rank 1, eight for rank 0); 1: FP8 cache
 // (p.kv_fp8; tensor maps unused).
 template <int kMode>
 cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
