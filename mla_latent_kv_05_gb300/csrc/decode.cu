@@ -187,6 +187,36 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (x0, x1) <- ((x0 - m) * c, (x1 - m) * c) with packed fp32x2 arithmetic.
+// The subtraction comes first, so x == m gives exactly 0 however large the
+// magnitudes are.
+__device__ __forceinline__ void sub_scale2(float& x0, float& x1, float neg_m, float c) {
+  asm("{\n\t.reg .b64 x, m, s;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 m, {%2, %2};\n\t"
+      "mov.b64 s, {%3, %3};\n\t"
+      "add.rn.f32x2 x, x, m;\n\t"
+      "mul.rn.f32x2 x, x, s;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(x0), "+f"(x1) : "f"(neg_m), "f"(c));
+}
+
+// (a0, a1) += (b0, b1), packed.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+
 // 32 e4m3 codes (8 words, lowest byte first) with their e8m0 scale byte ->
 // 16 bf16x2 words.  e4m3 -> f16 is exact in hardware, the product with the
 // power-of-two scale is exact in fp32 (no flush), and the result has at most
@@ -333,13 +363,22 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const int hp_end = 2 * sg.t1;
         for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
           const int nh = min(TH, hp_end - h0);
+          // The tile's block-table entries are read before the wait for free
+          // buffers, so their global-memory latency overlaps the wait instead
+          // of sitting between the copies (the copies' memory clobbers keep
+          // the compiler from hoisting them).
+          int pages[TH];
+#pragma unroll
+          for (int j = 0; j < TH; ++j) pages[j] = j < nh ? half_page(sg.b, h0 + j) : 0;
           if constexpr (kMode == 0) {
             // a bad page is read fully outside the tensor, which fills zeros
             if (rank == 1) {
               if (!wait_bounded<true>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
               ptx::mbar_arrive_expect_tx(BAR(KFULL + kb), static_cast<uint32_t>(nh) * kKSlot);
-              for (int j = 0; j < nh; ++j) {
-                const int hp = h0 + j, page = half_page(sg.b, hp);
+#pragma unroll
+              for (int j = 0; j < TH; ++j) {
+                if (j >= nh) break;
+                const int hp = h0 + j, page = pages[j];
                 if (page < 0) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
                 const int wq = (page < 0 ? p.num_pages : page) * 8 + (hp & 1) * 4;
                 ptx::tma_load_4d(sbase + static_cast<uint32_t>(kb * TH + j) * kKSlot, &tmap_k, BAR(KFULL + kb),
@@ -348,9 +387,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               kb ^= 1;
               if (kb == 0) kphase ^= 1u;
             } else {
-              for (int j = 0; j < nh; ++j) {
+#pragma unroll
+              for (int j = 0; j < TH; ++j) {
+                if (j >= nh) break;
                 if (!wait_bounded<true>(BAR(VEMPTY + vs), vphase ^ 1u, hdr)) { ok = false; break; }
-                const int hp = h0 + j, page = half_page(sg.b, hp);
+                const int hp = h0 + j, page = pages[j];
                 const int wq = (page < 0 ? p.num_pages : page) * 8 + (hp & 1) * 4;
                 ptx::mbar_arrive_expect_tx(BAR(VFULL + vs), kVSlot);
                 ptx::tma_load_4d(sbase + static_cast<uint32_t>(vs) * kVSlot, &tmap_v, BAR(VFULL + vs), 0, 0, 0, wq,
@@ -360,9 +401,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             }
           } else {
             // raw half pages; a bad page is never read (dequant writes zeros)
-            for (int j = 0; j < nh; ++j) {
+#pragma unroll
+            for (int j = 0; j < TH; ++j) {
+              if (j >= nh) break;
               if (!wait_bounded<true>(BAR(RAWEMPTY + rs), rphase ^ 1u, hdr)) { ok = false; break; }
-              const int hp = h0 + j, page = half_page(sg.b, hp);
+              const int hp = h0 + j, page = pages[j];
               if (page < 0 && rank == 1) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
               raw_flag[rs] = page < 0 ? 1u : 0u;
               if (page < 0) {
@@ -636,11 +679,17 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         // row max of the masked raw scores.  m_ref stays in raw score units and
         // P = exp2((s - m_ref) * c), so the max element gets exactly exp2(0) = 1
         // whatever the magnitude of the scores (scale c > 0).
+        const bool full = valid >= kN;                 // the same for every head of the tile
         float mx = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < kHC; ++e) {
-          if (c_mine + e < valid) mx = fmaxf(mx, __uint_as_float(mine[e]));
-          if (c_other + e < valid) mx = fmaxf(mx, __uint_as_float(other[e]));
+          for (int e = 0; e < kHC; ++e) mx = max3(mx, __uint_as_float(mine[e]), __uint_as_float(other[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHC; ++e) {
+            if (c_mine + e < valid) mx = fmaxf(mx, __uint_as_float(mine[e]));
+            if (c_other + e < valid) mx = fmaxf(mx, __uint_as_float(other[e]));
+          }
         }
         float alpha = 1.f;
         if (h0 == 2 * sg.t0) {
@@ -651,14 +700,28 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           m_ref = mx;
         }
         uint32_t pk[kHC / 2];
+        float la = 0.f, lb = 0.f;
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < kHC / 2; ++e) {
-          const int col = c_mine + 2 * e;
-          const float p0 = col < valid ? fast_exp2((__uint_as_float(mine[2 * e]) - m_ref) * c) : 0.f;
-          const float p1 = col + 1 < valid ? fast_exp2((__uint_as_float(mine[2 * e + 1]) - m_ref) * c) : 0.f;
-          pk[e] = pack_bf16x2(p0, p1);
-          l += p0 + p1;
+          for (int e = 0; e < kHC / 2; ++e) {
+            float x0 = __uint_as_float(mine[2 * e]), x1 = __uint_as_float(mine[2 * e + 1]);
+            sub_scale2(x0, x1, -m_ref, c);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            pk[e] = pack_bf16x2(p0, p1);
+            add2(la, lb, p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHC / 2; ++e) {
+            const int col = c_mine + 2 * e;
+            const float p0 = col < valid ? fast_exp2((__uint_as_float(mine[2 * e]) - m_ref) * c) : 0.f;
+            const float p1 = col + 1 < valid ? fast_exp2((__uint_as_float(mine[2 * e + 1]) - m_ref) * c) : 0.f;
+            pk[e] = pack_bf16x2(p0, p1);
+            la += p0;
+            lb += p1;
+          }
         }
+        l += la + lb;
         if (m_ref == -INFINITY) l = 0.f;     // nothing visible yet (every p was 0)
         if (!wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr)) { ok = false; break; }
         // This group's columns of P row h (kHC/8 pieces of 16 B: piece q holds
