@@ -107,14 +107,20 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   p.lse = lse;
   p.ws = static_cast<uint8_t*>(workspace);
   p.L = L;
+  // The three kernels are chained with programmatic dependent launch, so the
+  // attention kernel's prologue overlaps the planner and the merge kernel's
+  // launch overlaps the attention kernel's tail.  A call with the profiling
+  // hook set records its events between the kernels and launches them
+  // without that overlap, so that the events bracket the attention kernel.
   cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
   g_prof_before = g_prof_after = nullptr;
+  const bool pdl = ev0 == nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  const cudaError_t le =
-      fp8 ? launch_decode_fp8(p, ppg * sq, stream) : launch_decode_bf16(tmap_k, tmap_v, p, ppg * sq, stream);
+  const cudaError_t le = fp8 ? launch_decode_fp8(p, ppg * sq, pdl, stream)
+                             : launch_decode_bf16(tmap_k, tmap_v, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 

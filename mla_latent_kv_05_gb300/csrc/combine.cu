@@ -18,6 +18,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ row_index,
                                                       const int32_t* __restrict__ n_rows_dev, int n_rows,
                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  // launched as a programmatic dependent of the attention kernel: its
+  // partials are read only after that grid has completed
+  ptx::grid_dep_wait();
   const int k = blockIdx.x;
   const int rows = n_rows_dev ? *n_rows_dev : n_rows;
   if (k >= rows) return;
@@ -69,15 +72,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 // Merge of the decode plan's split rows (row list and count on the device).
 cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows, __nv_bfloat16* out, float* lse,
-                                cudaStream_t stream) {
+                                bool pdl, cudaStream_t stream) {
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   if (max_rows <= 0) return cudaSuccess;
-  combine_kernel<<<dim3(max_rows, kHeads / 8), 256, 0, stream>>>(
-      reinterpret_cast<const float*>(w + Lw.part_out), reinterpret_cast<const float*>(w + Lw.part_lse),
-      reinterpret_cast<const int32_t*>(w + Lw.comb_start), reinterpret_cast<const int32_t*>(w + Lw.comb_count),
-      reinterpret_cast<const int32_t*>(w + Lw.comb_row),
-      reinterpret_cast<const int32_t*>(w + offsetof(PlanHeader, n_comb)), 0, out, lse);
-  return cudaGetLastError();
+  // programmatic dependent launch: the kernel's launch overlaps the tail of
+  // the attention kernel; griddepcontrol.wait orders its reads after it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(max_rows, kHeads / 8, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, reinterpret_cast<const float*>(w + Lw.part_out),
+                            reinterpret_cast<const float*>(w + Lw.part_lse),
+                            reinterpret_cast<const int32_t*>(w + Lw.comb_start),
+                            reinterpret_cast<const int32_t*>(w + Lw.comb_count),
+                            reinterpret_cast<const int32_t*>(w + Lw.comb_row),
+                            reinterpret_cast<const int32_t*>(w + offsetof(PlanHeader, n_comb)), 0, out, lse);
 }
 
 // Public merge: parts of row r are [indptr[r], indptr[r+1]).

@@ -77,7 +77,7 @@ constexpr int kMaxVSlots = 5, kMaxRaw = 4;
 //   bf16: rank 1 = 6 K slots (two 3-slot tiles); rank 0 = 5 V slots + 2 P
 //         slots of two chunks (96 tokens).
 //   FP8:  rank 1 = 4 K slots (two 2-slot tiles) + 4 raw half pages; rank 0 =
-//         3 V slots + 2 one-chunk P slots + 3 raw half pages.
+//         4 V slots + 2 one-chunk P slots + 3 raw half pages.
 template <int kMode> struct Cfg;
 template <> struct Cfg<0> {
   static constexpr int kTileHalves = 3;
@@ -90,10 +90,12 @@ template <> struct Cfg<0> {
   static constexpr uint32_t kEnd0 = kOffP + kPSlots * kPSlotBytes;
   static constexpr uint32_t kOffMisc = kEnd1 > kEnd0 ? kEnd1 : kEnd0;
   static constexpr int kThreads = 384;
+  static constexpr int kSmGroups = 2;          // softmax warp groups (4 warps each)
+  static constexpr int kDqWarp0 = 0, kDqWarps = 0;
 };
 template <> struct Cfg<1> {
   static constexpr int kTileHalves = 2;
-  static constexpr int kVSlots = 3;
+  static constexpr int kVSlots = 4;
   static constexpr int kRaw1 = 4, kRaw0 = 3;
   static constexpr uint32_t kPSlotBytes = kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;
@@ -103,6 +105,8 @@ template <> struct Cfg<1> {
   static constexpr uint32_t kEnd0 = kOffRaw0 + kRaw0 * kRawBytes;
   static constexpr uint32_t kOffMisc = ((kEnd1 > kEnd0 ? kEnd1 : kEnd0) + 127) & ~127u;
   static constexpr int kThreads = 512;
+  static constexpr int kSmGroups = 1;          // 64-token tiles: one group of 4 warps takes all columns
+  static constexpr int kDqWarp0 = 8, kDqWarps = 8;   // 8 warps x at most 3 groups >= 18 groups
 };
 constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
 constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
@@ -127,6 +131,7 @@ static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared me
 static_assert(Cfg<0>::kVSlots <= kMaxVSlots && Cfg<1>::kVSlots <= kMaxVSlots, "V slot barriers");
 static_assert(Cfg<1>::kRaw1 <= kMaxRaw && Cfg<1>::kRaw0 <= kMaxRaw, "raw barriers");
 static_assert(Cfg<0>::kOffMisc % 1024 == 0, "slot alignment");
+static_assert(3 * Cfg<1>::kDqWarps >= kRow / 32, "each FP8 dequant warp takes at most three value groups");
 
 // TMEM columns.
 constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
@@ -275,7 +280,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   using C = Cfg<kMode>;
   constexpr int TH = C::kTileHalves;            // half pages per tile
   constexpr int kN = TH * kHalf;                // tokens per tile (S columns)
-  constexpr int kHC = kN / 2;                   // S columns per softmax group
+  constexpr int kSG = C::kSmGroups;             // softmax warp groups
+  constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
   constexpr uint32_t kIdescS = ptx::idesc_bf16(128, kN, 0, 0);   // A = Q (TMEM), B = K (K-major)
   constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
@@ -306,15 +312,17 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
 
   const bool smem_ok = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
-    if (!smem_ok) set_status(&hdr->status, MLA_ERR_UNSUPPORTED);
     // K tiles: the TMA bytes (bf16) or the four dequant warps (FP8)
-    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : 4u); ptx::mbar_init(BAR(KEMPTY + s), 1); }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : static_cast<uint32_t>(C::kDqWarps));
+      ptx::mbar_init(BAR(KEMPTY + s), 1);
+    }
     for (int s = 0; s < kMaxVSlots; ++s) {
-      ptx::mbar_init(BAR(VFULL + s), kMode == 0 ? 1u : 4u);
+      ptx::mbar_init(BAR(VFULL + s), kMode == 0 ? 1u : static_cast<uint32_t>(C::kDqWarps));
       ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
-    for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 256); ptx::mbar_init(BAR(PEMPTY + s), 1); }
-    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 256); }
+    for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
+    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128 * kSG); }
     ptx::mbar_init(BAR(QREADY), 128);
     ptx::mbar_init(BAR(REQ), 2);
     ptx::mbar_init(BAR(CORR), 4);
@@ -322,7 +330,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     ptx::mbar_init(BAR(OEMPTY), 128);
     ptx::mbar_init(BAR(LSUM), 128);
     for (int s = 0; s < kMailSlots; ++s) { ptx::mbar_init(BAR(MBFULL + s), 128); ptx::mbar_init(BAR(MBEMPTY + s), 4); }
-    for (int s = 0; s < kMaxRaw; ++s) { ptx::mbar_init(BAR(RAWFULL + s), 1); ptx::mbar_init(BAR(RAWEMPTY + s), 4); }
+    for (int s = 0; s < kMaxRaw; ++s) {
+      ptx::mbar_init(BAR(RAWFULL + s), 1);
+      ptx::mbar_init(BAR(RAWEMPTY + s), kMode == 0 ? 1u : static_cast<uint32_t>(C::kDqWarps));
+    }
     ptx::fence_barrier_init();
   }
   if (warp == 2) {
@@ -335,6 +346,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   ptx::tc_fence_after();
   ptx::cluster_sync();   // barriers of both ranks initialised before any remote arrive
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
+  // Everything above overlaps the planner when this grid is its programmatic
+  // dependent; the plan is read only after the planner grid has completed.
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();   // the merge kernel may begin launching
+  if (threadIdx.x == 0 && !smem_ok) set_status(&hdr->status, MLA_ERR_UNSUPPORTED);
 
   const int ppg = hdr->pairs_per_group;
   const int group = static_cast<int>(pair) / ppg;     // query index i served by this pair
@@ -361,15 +377,21 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       bool ok = true;
       while (ok && w.next(sg)) {
         const int hp_end = 2 * sg.t1;
+        // Block-table entries are read one tile ahead, so their global-memory
+        // latency overlaps the previous tile's waits and copies instead of
+        // sitting between the copies (the copies' memory clobbers keep the
+        // compiler from hoisting the reads on its own).
+        int next_pages[TH];
+#pragma unroll
+        for (int j = 0; j < TH; ++j) next_pages[j] = 2 * sg.t0 + j < hp_end ? half_page(sg.b, 2 * sg.t0 + j) : 0;
         for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
           const int nh = min(TH, hp_end - h0);
-          // The tile's block-table entries are read before the wait for free
-          // buffers, so their global-memory latency overlaps the wait instead
-          // of sitting between the copies (the copies' memory clobbers keep
-          // the compiler from hoisting them).
           int pages[TH];
 #pragma unroll
-          for (int j = 0; j < TH; ++j) pages[j] = j < nh ? half_page(sg.b, h0 + j) : 0;
+          for (int j = 0; j < TH; ++j) {
+            pages[j] = next_pages[j];
+            next_pages[j] = h0 + TH + j < hp_end ? half_page(sg.b, h0 + TH + j) : 0;
+          }
           if constexpr (kMode == 0) {
             // a bad page is read fully outside the tensor, which fills zeros
             if (rank == 1) {
@@ -422,17 +444,15 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
       }
     }
-  } else if (kMode == 1 && active && warp >= 12) {
-    // ------------------------------------------------------------ FP8 dequant (warps 12..15)
-    // raw half page -> one bf16 slot (32 tokens).  Warp wq handles tokens of
-    // parity (wq & 1) (so the row's 2-byte misalignment is warp-uniform) and
-    // half of the 32-value groups (9 of 18 on rank 1, 8 of the 16 latent
-    // groups on rank 0).
-    const int wq = warp - 12;
-    const int parity = wq & 1;
-    const int G = rank == 1 ? 9 : 8;
-    const int g0 = (wq >> 1) * G;
-    const int n_tasks = 16 * G;
+  } else if (kMode == 1 && active && warp >= C::kDqWarp0) {
+    // ------------------------------------------------------------ FP8 dequant (warps 8..15)
+    // raw half page -> one bf16 slot (32 tokens).  Lane = token, so the 32
+    // lanes' 16-byte stores of one value group hit 32 different swizzled
+    // rows (conflict-free per 8 rows); warp wq of 8 takes value groups wq,
+    // wq+8, ... (18 groups on rank 1, the 16 latent groups on rank 0).
+    constexpr int kDW = C::kDqWarps;
+    const int wq = warp - C::kDqWarp0;
+    const int G2 = rank == 1 ? 18 : 16;
     const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
     const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
     const uint32_t gstride = rank == 1 ? kKGroup : kVGroup;
@@ -458,18 +478,24 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           }
           if (!wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
           const bool zero = raw_flag[rs] != 0;
-          const uint8_t* raw = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes;
-          for (int task = lane; task < n_tasks; task += 32) {
-            const int tok = 2 * (task / G) + parity;          // token within the half page
-            const int g = g0 + task % G;                       // 32-value group
-            uint32_t o[16];
+          const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + lane * kFp8Row;
+          {
+            // groups wq, wq+8 and (rank 1, wq < 2) wq+16: one pass, three
+            // independent chains
+            const int ga = wq, gb = wq + kDW, gc = wq + 2 * kDW;
+            const bool hb = gb < G2, hc = gc < G2;
+            uint32_t o0[16], o1[16], o2[16];
             if (!zero) {
-              dequant_group(raw + tok * kFp8Row, g, o);
+              dequant_group(row, ga, o0);
+              if (hb) dequant_group(row, gb, o1);
+              if (hc) dequant_group(row, gc, o2);
             } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = 0u;
+              for (int i = 0; i < 16; ++i) { o0[i] = 0u; o1[i] = 0u; o2[i] = 0u; }
             }
-            store_group(slot, gstride, tok, g, o);
+            store_group(slot, gstride, lane, ga, o0);
+            if (hb) store_group(slot, gstride, lane, gb, o1);
+            if (hc) store_group(slot, gstride, lane, gc, o2);
           }
           ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA (async proxy)
           __syncwarp();
@@ -608,12 +634,13 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       }
       first_seg = false;
     }
-  } else if (active && warp >= 4 && warp < 12 && rank == 1) {
+  } else if (active && warp >= 4 && warp < 4 + 4 * kSG && rank == 1) {
     // ------------------------------------------------------------ softmax (thread = head)
-    // Group 0 (warps 4..7) turns columns [0, kHC) of each tile's S into P,
-    // group 1 (warps 8..11) columns [kHC, kN).  Both take the row max over all
-    // kN columns, so their reference maxima and rescale factors agree without
-    // an exchange; the two partial sums meet once per segment (LSUM barrier).
+    // bf16 (two groups): group 0 (warps 4..7) turns columns [0, kHC) of each
+    // tile's S into P, group 1 (warps 8..11) columns [kHC, kN).  Both take the
+    // row max over all kN columns, so their reference maxima and rescale
+    // factors agree without an exchange; the two partial sums meet once per
+    // segment (LSUM barrier).  FP8 (one group): warps 4..7 take all columns.
     const int grp = (warp - 4) >> 2;
     const int h = (threadIdx.x - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -663,11 +690,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         ptx::tc_fence_after();
         const uint32_t sadr = tmem + lane_base + kSCol + static_cast<uint32_t>(kN * sb);
         const int c_mine = kHC * grp, c_other = kHC * (grp ^ 1);
-        uint32_t mine[kHC], other[kHC];
+        uint32_t mine[kHC], other[kSG == 2 ? kHC : 1];
 #pragma unroll
         for (int j = 0; j < kHC / 16; ++j) {
           ptx::tmem_ld16(sadr + c_mine + 16 * j, mine + 16 * j);
-          ptx::tmem_ld16(sadr + c_other + 16 * j, other + 16 * j);
+          if constexpr (kSG == 2) ptx::tmem_ld16(sadr + c_other + 16 * j, other + 16 * j);
         }
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
@@ -682,13 +709,19 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const bool full = valid >= kN;                 // the same for every head of the tile
         float mx = -INFINITY;
         if (full) {
+          if constexpr (kSG == 2) {
 #pragma unroll
-          for (int e = 0; e < kHC; ++e) mx = max3(mx, __uint_as_float(mine[e]), __uint_as_float(other[e]));
+            for (int e = 0; e < kHC; ++e) mx = max3(mx, __uint_as_float(mine[e]), __uint_as_float(other[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < kHC; e += 2) mx = max3(mx, __uint_as_float(mine[e]), __uint_as_float(mine[e + 1]));
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < kHC; ++e) {
             if (c_mine + e < valid) mx = fmaxf(mx, __uint_as_float(mine[e]));
-            if (c_other + e < valid) mx = fmaxf(mx, __uint_as_float(other[e]));
+            if constexpr (kSG == 2)
+              if (c_other + e < valid) mx = fmaxf(mx, __uint_as_float(other[e]));
           }
         }
         float alpha = 1.f;
@@ -743,14 +776,16 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
       if (!ok) break;
-      if (grp == 1) {
+      if (kSG == 2 && grp == 1) {
         // hand group 1's partial sum to group 0 (read before group 0 loads the
         // next segment's Q, so group 1 cannot overwrite it early)
         l_part[h] = l;
         ptx::mbar_arrive(BAR(LSUM));
       } else {
-        if (!wait_warp<false>(BAR(LSUM), lsum_phase, hdr)) { ok = false; break; }
-        l += l_part[h];
+        if constexpr (kSG == 2) {
+          if (!wait_warp<false>(BAR(LSUM), lsum_phase, hdr)) { ok = false; break; }
+          l += l_part[h];
+        }
         const bool split = slot_base[sg.b] >= 0;
         const int slot = split ? group * spq + slot_base[sg.b] + (pl - first_pair[sg.b]) : -1;
         const float lse_v = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -INFINITY;
@@ -889,7 +924,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
 // (p.kv_fp8; tensor maps unused).
 template <int kMode>
 cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
-                               int n_pairs, cudaStream_t stream) {
+                               int n_pairs, bool pdl, cudaStream_t stream) {
   auto kern = mla_decode_pair_kernel<kMode>;
   static int configured_device = -1;
   int dev = 0;
@@ -904,20 +939,23 @@ cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tma
   cfg.blockDim = dim3(dk::Cfg<kMode>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = dk::smem_bytes<kMode>();
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tmap_k, tmap_v, p);
 }
 
 cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
-                               int n_pairs, cudaStream_t stream) {
-  return launch_decode_mode<0>(tmap_k, tmap_v, p, n_pairs, stream);
+                               int n_pairs, bool pdl, cudaStream_t stream) {
+  return launch_decode_mode<0>(tmap_k, tmap_v, p, n_pairs, pdl, stream);
 }
 
-cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, cudaStream_t stream) {
+cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return launch_decode_mode<1>(unused, unused, p, n_pairs, stream);
+  return launch_decode_mode<1>(unused, unused, p, n_pairs, pdl, stream);
 }
 
 int decode_max_pairs() {

@@ -22,12 +22,14 @@ struct DecodeParams {
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_pages, int pairs_per_group,
                         void* ws, const WsLayout& L, cudaStream_t stream);
+// pdl: launch as a programmatic dependent of the planner (the kernel waits on
+// griddepcontrol before reading the plan)
 cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
-                               int n_pairs, cudaStream_t stream);
-cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, cudaStream_t stream);
+                               int n_pairs, bool pdl, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 int decode_max_pairs();
 cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows, __nv_bfloat16* out, float* lse,
-                                cudaStream_t stream);
+                                bool pdl, cudaStream_t stream);
 cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,
                                   __nv_bfloat16* out, float* lse, cudaStream_t stream);
 

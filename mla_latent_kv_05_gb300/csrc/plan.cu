@@ -58,6 +58,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   int* comb_count = reinterpret_cast<int*>(ws + L.comb_count);
 
   const int tid = threadIdx.x;
+  // the attention kernel may begin its prologue now; it reads the plan only
+  // after this grid has completed (griddepcontrol.wait)
+  ptx::grid_dep_launch();
   const int per = (batch + blockDim.x - 1) / blockDim.x;
   const int lo = min(batch, tid * per), hi = min(batch, lo + per);
   const int max_len = max_pages * kPage;

@@ -60,6 +60,17 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
                :: "r"(addr), "r"(v), "r"(bar) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grids this launch depends on have completed and their
+// memory is visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the dependent launch that follows in the stream begin its prologue.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
