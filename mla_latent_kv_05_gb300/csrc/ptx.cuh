@@ -152,6 +152,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                " [%0], [%1], %2, [%3], %4;"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
+// Bulk copy from this CTA's shared memory (src, a shared::cta address) into
+// the shared memory of a CTA of the cluster (dst, a shared::cluster address
+// from mapa); the bytes are counted on `bar`, an mbarrier in the destination
+// CTA (also a shared::cluster address).  Both addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2s(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
+}
 // Prefetch a contiguous global range (16-byte aligned, multiple of 16 B) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");

@@ -141,7 +141,7 @@ def test_growing_scores_exercise_rescale(cuda_device):
     pages = inp.block_table[0, : (n + 63) // 64]
     for j in range(n):
         inp.kv_cache[pages[j // 64], j % 64, 0] = j * 0.02
-    inp.q_absorbed[..., 0] = torch.linspace(1, 60, 128).to(torch.bfloat16)
+    inp.q_absorbed[..., 0] = torch.linspace(1, 120, 128).to(torch.bfloat16)
     out, lse, st = run_gpu(inp)
     assert st == 0
     assert_close(out, lse, *oracle(inp))
