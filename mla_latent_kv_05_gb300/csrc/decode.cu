@@ -830,8 +830,14 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         // tokens 8q..8q+7, in chunk q/8 at swizzled position (q%8) ^ (h%8)) --
         // and, from group 0, alpha_h -- go to rank 0 as st.async bytes counted
         // on its PFULL barrier: nobody waits for them here.
+        // alpha of heads 4i..4i+3 gathered into lane i (< 8) of each group-0
+        // warp, sent as one 16-byte store per lane
+        float a4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a4[k] = __shfl_sync(0xffffffffu, alpha, ((lane & 7) << 2) + k);
+        const bool sends_alpha = grp == 0 && lane < 8;
         const uint32_t pfull = ptx::mapa(BAR(PFULL + ps), 0);
-        ptx::mbar_arrive_expect_tx_remote(pfull, grp == 0 ? 2u * kHC + 4u : 2u * kHC);
+        ptx::mbar_arrive_expect_tx_remote(pfull, 2u * kHC + (sends_alpha ? 16u : 0u));
         const uint32_t prow = ptx::mapa(sbase + C::kOffP + static_cast<uint32_t>(ps) * C::kPSlotBytes + h * 128u, 0);
 #pragma unroll
         for (int j = 0; j < kHC / 8; ++j) {
@@ -839,8 +845,9 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           ptx::st_async_v4(prow + static_cast<uint32_t>(q >> 3) * kPChunk + ((static_cast<uint32_t>(q & 7) ^ (h & 7)) << 4),
                            pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], pfull);
         }
-        if (grp == 0)
-          ptx::st_async_b32(ptx::mapa(sbase + kOffAlpha + ps * 512u + h * 4u, 0), __float_as_uint(alpha), pfull);
+        if (sends_alpha)
+          ptx::st_async_v4(ptx::mapa(sbase + kOffAlpha + ps * 512u + (h + 3 * lane) * 4u, 0), __float_as_uint(a4[0]),
+                           __float_as_uint(a4[1]), __float_as_uint(a4[2]), __float_as_uint(a4[3]), pfull);
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
