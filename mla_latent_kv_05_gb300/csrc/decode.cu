@@ -207,24 +207,16 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // The subtraction comes first, so x == m gives exactly 0 however large the
 // magnitudes are.
 __device__ __forceinline__ void sub_scale2(float& x0, float& x1, float neg_m, float c) {
-  asm("{\n\t.reg .b64 x, m, s;\n\t"
-      "mov.b64 x, {%0, %1};\n\t"
-      "mov.b64 m, {%2, %2};\n\t"
-      "mov.b64 s, {%3, %3};\n\t"
-      "add.rn.f32x2 x, x, m;\n\t"
-      "mul.rn.f32x2 x, x, s;\n\t"
-      "mov.b64 {%0, %1}, x;\n\t}"
-      : "+f"(x0), "+f"(x1) : "f"(neg_m), "f"(c));
+  const float2 v = __fmul2_rn(__fadd2_rn(make_float2(x0, x1), make_float2(neg_m, neg_m)), make_float2(c, c));
+  x0 = v.x;
+  x1 = v.y;
 }
 
 // (a0, a1) += (b0, b1), packed.
 __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 a, b;\n\t"
-      "mov.b64 a, {%0, %1};\n\t"
-      "mov.b64 b, {%2, %3};\n\t"
-      "add.rn.f32x2 a, a, b;\n\t"
-      "mov.b64 {%0, %1}, a;\n\t}"
-      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+  const float2 v = __fadd2_rn(make_float2(a0, a1), make_float2(b0, b1));
+  a0 = v.x;
+  a1 = v.y;
 }
 
 // 32 e4m3 codes (8 words, lowest byte first) with their e8m0 scale byte ->
