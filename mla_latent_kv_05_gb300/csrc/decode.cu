@@ -443,6 +443,21 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
             }
           }
+          if (rank == 1 && h0 + TH >= hp_end) {
+            // The segment's last tile is on its way: bring the next segment's
+            // query rows (128 KiB absorbed + 16 KiB RoPE, each contiguous)
+            // into L2, so the softmax warps' Q load a few tiles later hits L2.
+            SegWalker w2 = w;
+            Segment nx;
+            if (w2.next(nx)) {
+              const size_t qrow = static_cast<size_t>(nx.b) * sq + group;
+              const uint8_t* qa = reinterpret_cast<const uint8_t*>(p.q_abs + qrow * kHeads * kDc);
+              const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope + qrow * kHeads * kDr);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) ptx::prefetch_l2_bulk(qa + k * 32768, 32768);
+              ptx::prefetch_l2_bulk(qr, kHeads * kDr * 2);
+            }
+          }
         }
       }
     }
@@ -947,19 +962,19 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       const bool split = slot_base[sg.b] >= 0;
       if (split) {
         const int slot = group * spq + slot_base[sg.b] + (pl - first_pair[sg.b]);
-        float4* dst = reinterpret_cast<float4*>(part_out + (static_cast<size_t>(slot) * kHeads + h) * kDc);
+        float* dst = part_out + (static_cast<size_t>(slot) * kHeads + h) * kDc;
 #pragma unroll 1
         for (int cc = c0; cc < c0 + 8; ++cc) {
           uint32_t r[32];
           ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[cc * 8 + v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
-                                          __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * inv_l);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) ptx::st_global_v8(dst + cc * 32 + v * 8, r + 8 * v);   // whole 32-byte sectors
         }
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(row) * kHeads + h) * kDc);
+        __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
 #pragma unroll 1
         for (int cc = c0; cc < c0 + 8; ++cc) {
           uint32_t r[32];
@@ -968,8 +983,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           uint32_t o[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) dst[cc * 4 + v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          ptx::st_global_v8(dst + cc * 32, o);
+          ptx::st_global_v8(dst + cc * 32 + 16, o + 8);
         }
       }
       ptx::tc_fence_before();
