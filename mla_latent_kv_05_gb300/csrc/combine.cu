@@ -1,7 +1,10 @@
 // Split-KV merge.  Attention over disjoint token sets combines exactly from
 // each part's normalised output and LSE:
 //     L = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - L) * out_s.
-// One warp per (output row, head), 16 fp32 per lane (float4 loads), bf16 out.
+// One warp per (output row, head), 16 values per lane, bf16 out.  The
+// decode plan's partials are bf16 (each part already normalised, so its
+// rounding adds at most 2^-9 relative to the merge); the public entry point
+// merges fp32 partials.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -10,8 +13,21 @@ namespace mla {
 
 namespace {
 
-// grid (rows, 128 / 8): one warp per (row, head); 16 fp32 per lane.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
+__device__ __forceinline__ void load4(const float* src, int i, float* x) {
+  const float4 v = __ldcs(reinterpret_cast<const float4*>(src) + i);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* src, int i, float* x) {
+  const uint2 v = __ldcs(reinterpret_cast<const uint2*>(src) + i);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// grid (rows, 128 / 8): one warp per (row, head); lane holds values
+// 4(32q + lane) .. +3 for q = 0..3.
+template <typename TP>
+__global__ void __launch_bounds__(256) combine_kernel(const TP* __restrict__ part_out,
                                                       const float* __restrict__ part_lse,
                                                       const int32_t* __restrict__ row_start,
                                                       const int32_t* __restrict__ row_count,
@@ -43,15 +59,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       const float v = part_lse[static_cast<size_t>(start + s) * kHeads + h];
       const float wgt = v == -INFINITY ? 0.f : __expf(v - L);
       sum += wgt;
-      const float4* src = reinterpret_cast<const float4*>(part_out + (static_cast<size_t>(start + s) * kHeads + h) * kDc);
-      float4 x[4];
+      const TP* src = part_out + (static_cast<size_t>(start + s) * kHeads + h) * kDc;
+      float x[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) x[q] = __ldcs(src + q * 32 + lane);
+      for (int q = 0; q < 4; ++q) load4(src, q * 32 + lane, x + 4 * q);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[4 * q] += wgt * x[q].x; acc[4 * q + 1] += wgt * x[q].y;
-        acc[4 * q + 2] += wgt * x[q].z; acc[4 * q + 3] += wgt * x[q].w;
-      }
+      for (int e = 0; e < 16; ++e) acc[e] += wgt * x[e];
     }
   }
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
@@ -87,7 +100,7 @@ cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, reinterpret_cast<const float*>(w + Lw.part_out),
+  return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, reinterpret_cast<const __nv_bfloat16*>(w + Lw.part_out),
                             reinterpret_cast<const float*>(w + Lw.part_lse),
                             reinterpret_cast<const int32_t*>(w + Lw.comb_start),
                             reinterpret_cast<const int32_t*>(w + Lw.comb_count),
@@ -99,7 +112,8 @@ cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows
 cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,
                                   __nv_bfloat16* out, float* lse, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  combine_kernel<<<dim3(rows, kHeads / 8), 256, 0, stream>>>(part_out, part_lse, indptr, nullptr, nullptr, nullptr, rows, out, lse);
+  combine_kernel<float><<<dim3(rows, kHeads / 8), 256, 0, stream>>>(part_out, part_lse, indptr, nullptr, nullptr, nullptr,
+                                                                    rows, out, lse);
   return cudaGetLastError();
 }
 

@@ -54,7 +54,7 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs) {
   L.comb_start = o;  o = align256(o + sizeof(int) * batch * sq);
   L.comb_count = o;  o = align256(o + sizeof(int) * batch * sq);
   L.part_lse = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads);
-  L.part_out = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads * kDc);
+  L.part_out = o;    o = align256(o + 2 * static_cast<size_t>(L.max_slots) * kHeads * kDc);   // bf16 partials
   L.total = o;
   return L;
 }

@@ -267,6 +267,27 @@ __device__ __forceinline__ void store_group(uint8_t* slot, uint32_t group_stride
   }
 }
 
+// Load 32-column chunks [C0, C1) of one head's query row (chunk c < 8: the
+// absorbed query at byte 128c, chunk 8: the RoPE query) with 32-byte loads
+// and store them into the TMEM lane row at column 32c (two bf16 per column).
+// Two chunks per round trip.
+template <int C0, int C1>
+__device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* qr, uint32_t taddr) {
+#pragma unroll 1
+  for (int c = C0; c < C1; c += 2) {
+    uint32_t r0[32], r1[32];
+    const bool two = c + 1 < C1;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) ptx::ld_global_nc_v8((c < 8 ? qa + c * 128 : qr) + 32 * v, r0 + 8 * v);
+    if (two) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) ptx::ld_global_nc_v8((c + 1 < 8 ? qa + (c + 1) * 128 : qr) + 32 * v, r1 + 8 * v);
+    }
+    ptx::tmem_st32(taddr + 32u * c, r0);
+    if (two) ptx::tmem_st32(taddr + 32u * (c + 1), r1);
+  }
+}
+
 }  // namespace dk
 
 template <int kMode>   // 0: bf16 cache via TMA, 1: FP8 cache via bulk copies + dequant
@@ -299,7 +320,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const int* first_pair = reinterpret_cast<const int*>(p.ws + p.L.first_pair);
   const int* slot_base = reinterpret_cast<const int*>(p.ws + p.L.slot_base);
   float* part_lse = reinterpret_cast<float*>(p.ws + p.L.part_lse);
-  float* part_out = reinterpret_cast<float*>(p.ws + p.L.part_out);
+  __nv_bfloat16* part_out = reinterpret_cast<__nv_bfloat16*>(p.ws + p.L.part_out);
   auto BAR = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
   // physical page of row-local half page hp of batch row b (or -1 if out of range)
   auto half_page = [&](int b, int hp) -> int {
@@ -324,7 +345,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
     for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128 * kSG); }
-    ptx::mbar_init(BAR(QREADY), 128);
+    ptx::mbar_init(BAR(QREADY), 128 * kSG);
     ptx::mbar_init(BAR(REQ), 2);
     ptx::mbar_init(BAR(CORR), 8);
     ptx::mbar_init(BAR(OFULL), 1);
@@ -732,29 +753,18 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     while (ok && w.next(sg)) {
       const int row = sg.b * sq + group;
       const int len_i = lens[sg.b] - (sq - 1 - group);
-      if (grp == 0) {
-        // Q row h -> TMEM lane h, columns [0, 288): two bf16 per column, K order
-        const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<size_t>(row) * kHeads + h) * kDc);
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + (static_cast<size_t>(row) * kHeads + h) * kDr);
-#pragma unroll 1
-        for (int c3 = 0; c3 < 3; ++c3) {          // three chunks of 32 columns per round trip
-          uint4 x[24];
-#pragma unroll
-          for (int v = 0; v < 24; ++v) {
-            const int cc = c3 * 3 + v / 8;
-            x[v] = __ldg((cc < 8 ? qa + cc * 8 : qr) + (v & 7));
-          }
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            uint32_t r[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              r[4 * v] = x[8 * j + v].x; r[4 * v + 1] = x[8 * j + v].y;
-              r[4 * v + 2] = x[8 * j + v].z; r[4 * v + 3] = x[8 * j + v].w;
-            }
-            ptx::tmem_st32(tmem + lane_base + kQCol + 32u * (c3 * 3 + j), r);
-          }
-        }
+      {
+        // Q row h -> TMEM lane h, columns [0, 288): two bf16 per column, K
+        // order, 32 columns (128 B of the row) per chunk.  With two groups,
+        // group 0 loads chunks 0..4 and group 1 chunks 5..8; each reaches
+        // this point only after the previous segment's last S (which reads
+        // Q) has completed.
+        const uint8_t* qa = reinterpret_cast<const uint8_t*>(p.q_abs + (static_cast<size_t>(row) * kHeads + h) * kDc);
+        const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope + (static_cast<size_t>(row) * kHeads + h) * kDr);
+        const uint32_t qaddr = tmem + lane_base + kQCol;
+        if (kSG == 1) load_q_chunks<0, 9>(qa, qr, qaddr);
+        else if (grp == 0) load_q_chunks<0, 5>(qa, qr, qaddr);
+        else load_q_chunks<5, 9>(qa, qr, qaddr);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(BAR(QREADY));
@@ -959,33 +969,22 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       ptx::tc_fence_after();
       if (!wait_warp<true>(BAR(MBFULL + ms), mphase, hdr)) { ok = false; break; }
       const float inv_l = mail[ms * 128 + h];
+      // out = bf16(O / l): into the output row, or (split rows) into the
+      // row's partial slot, which the merge kernel combines
       const bool split = slot_base[sg.b] >= 0;
-      if (split) {
-        const int slot = group * spq + slot_base[sg.b] + (pl - first_pair[sg.b]);
-        float* dst = part_out + (static_cast<size_t>(slot) * kHeads + h) * kDc;
+      __nv_bfloat16* dst =
+          split ? part_out + (static_cast<size_t>(group * spq + slot_base[sg.b] + (pl - first_pair[sg.b])) * kHeads + h) * kDc
+                : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
 #pragma unroll 1
-        for (int cc = c0; cc < c0 + 8; ++cc) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
-          ptx::tmem_wait_ld();
+      for (int cc = c0; cc < c0 + 8; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
+        ptx::tmem_wait_ld();
+        uint32_t o[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * inv_l);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) ptx::st_global_v8(dst + cc * 32 + v * 8, r + 8 * v);   // whole 32-byte sectors
-        }
-      } else {
-        __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
-#pragma unroll 1
-        for (int cc = c0; cc < c0 + 8; ++cc) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
-          ptx::tmem_wait_ld();
-          uint32_t o[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-          ptx::st_global_v8(dst + cc * 32, o);
-          ptx::st_global_v8(dst + cc * 32 + 16, o + 8);
-        }
+        for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+        ptx::st_global_v8(dst + cc * 32, o);          // whole 32-byte sectors
+        ptx::st_global_v8(dst + cc * 32 + 16, o + 8);
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(BAR(OEMPTY));

@@ -60,6 +60,12 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
                :: "r"(addr), "r"(v), "r"(bar) : "memory");
 }
 
+// 32-byte read-only global load (address 32-byte aligned): one whole sector per lane.
+__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t* v) {
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
 // 32-byte global store (address 32-byte aligned): one whole sector per lane.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
