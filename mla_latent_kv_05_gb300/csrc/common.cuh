@@ -23,7 +23,7 @@ constexpr int kMaxRows = 1 << 16;   // batch * Sq handled by the planner
 struct PlanHeader {
   int status;            // first device-side problem seen (0 = none)
   int n_tiles;           // total KV tiles over the batch (longest query)
-  int chunk;             // tiles per pair
+  int chunk;             // mean pages per pair (information only; the ranges are pair_lo)
   int slots_per_query;   // partial slots of one query index
   int n_comb;            // rows the merge kernel must write
   int pairs_per_group;   // pairs that serve one query index
@@ -33,7 +33,7 @@ struct PlanHeader {
 
 // Offsets (bytes) of the plan arrays and split partials inside the workspace.
 struct WsLayout {
-  size_t lens, tile_start, first_pair, slot_base, comb_row, comb_start, comb_count;
+  size_t lens, tile_start, row_cost, pair_lo, pair_rank, first_pair, slot_base, comb_row, comb_start, comb_count;
   size_t part_lse, part_out, total;
   int max_slots;
 };
@@ -48,6 +48,9 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs) {
   size_t o = align256(sizeof(PlanHeader));
   L.lens = o;        o = align256(o + sizeof(int) * batch);
   L.tile_start = o;  o = align256(o + sizeof(int) * (batch + 1));
+  L.row_cost = o;    o = align256(o + sizeof(int) * (batch + 1));
+  L.pair_lo = o;     o = align256(o + sizeof(int) * (pg + 1));
+  L.pair_rank = o;   o = align256(o + sizeof(int) * (pg + 1));
   L.first_pair = o;  o = align256(o + sizeof(int) * batch);
   L.slot_base = o;   o = align256(o + sizeof(int) * batch);
   L.comb_row = o;    o = align256(o + sizeof(int) * batch * sq);

@@ -378,10 +378,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const int ppg = hdr->pairs_per_group;
   const int group = static_cast<int>(pair) / ppg;     // query index i served by this pair
   const int pl = static_cast<int>(pair) % ppg;
-  const int chunk = hdr->chunk;
-  const int n_tiles = hdr->n_tiles;
   const int spq = hdr->slots_per_query;
-  const int lo = min(pl * chunk, n_tiles), hi = min(lo + chunk, n_tiles);
+  const int* pair_lo = reinterpret_cast<const int*>(p.ws + p.L.pair_lo);
+  const int* pair_rank = reinterpret_cast<const int*>(p.ws + p.L.pair_rank);   // non-empty pairs before p
+  const int lo = pair_lo[pl], hi = pair_lo[pl + 1];     // this pair's page range (cost-balanced by the planner)
   const int sq = p.sq;
   const bool active = smem_ok && group < sq;
 
@@ -880,7 +880,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           l += l_part[h];
         }
         const bool split = slot_base[sg.b] >= 0;
-        const int slot = split ? group * spq + slot_base[sg.b] + (pl - first_pair[sg.b]) : -1;
+        const int slot = split ? group * spq + slot_base[sg.b] + (pair_rank[pl] - pair_rank[first_pair[sg.b]]) : -1;
         const float lse_v = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -INFINITY;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         if (split) part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
@@ -973,7 +973,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       // row's partial slot, which the merge kernel combines
       const bool split = slot_base[sg.b] >= 0;
       __nv_bfloat16* dst =
-          split ? part_out + (static_cast<size_t>(group * spq + slot_base[sg.b] + (pl - first_pair[sg.b])) * kHeads + h) * kDc
+          split ? part_out + (static_cast<size_t>(group * spq + slot_base[sg.b] + (pair_rank[pl] - pair_rank[first_pair[sg.b]])) * kHeads + h) * kDc
                 : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
 #pragma unroll 1
       for (int cc = c0; cc < c0 + 8; ++cc) {

@@ -3,19 +3,26 @@
 // slots of rows that end up split, and the list of rows the merge kernel
 // writes.  One CTA of 1024 threads.
 //
-// Partition: every batch row b has n_b = ceil(seq_len_b / 64) tiles (one tile
-// = one page).  The rows' tiles are laid end to end (prefix sums tile_start)
-// and cut into pieces of `chunk` = ceil(total / pairs_per_group) tiles; pair
-// p of a query group takes tiles [p*chunk, (p+1)*chunk).  Each query index
-// i < Sq has its own group of pairs with the identical partition, so the
-// groups read the same pages at about the same time and share them in L2.
-// A row covered by one pair is written straight to `out`; a row covered by
-// k > 1 pairs gets k partial slots (per query index) and a merge entry.
+// Partition: every batch row b has n_b = ceil(seq_len_b / 64) pages.  The
+// rows' pages are laid end to end (prefix sums tile_start) and cut into one
+// contiguous range per pair of a query group, [pair_lo[p], pair_lo[p+1]).
+// The cut balances cost, not pages: a pair's cost is its pages plus a fixed
+// cost for every row segment it starts (query load, output write, pipeline
+// refill), so a pair that crosses more row starts gets fewer pages.  Each
+// query index i < Sq has its own group of pairs with the identical
+// partition, so the groups read the same pages at about the same time and
+// share them in L2.  A row covered by one pair is written straight to `out`;
+// a row covered by k > 1 pairs gets k partial slots (per query index) and a
+// merge entry.
 #include "common.cuh"
 
 namespace mla {
 
 namespace {
+
+// Cost of starting a row segment, in pages: measured at 5-8 us per segment
+// against about 1.2 us per page on GB300.
+constexpr int kSegCost = 5;
 
 __device__ int block_exclusive_scan(int v, int* smem_warp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -51,6 +58,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
   int* lens = reinterpret_cast<int*>(ws + L.lens);
   int* tile_start = reinterpret_cast<int*>(ws + L.tile_start);
+  int* row_cost = reinterpret_cast<int*>(ws + L.row_cost);
+  int* pair_lo = reinterpret_cast<int*>(ws + L.pair_lo);
+  int* pair_rank = reinterpret_cast<int*>(ws + L.pair_rank);
   int* first_pair = reinterpret_cast<int*>(ws + L.first_pair);
   int* slot_base = reinterpret_cast<int*>(ws + L.slot_base);
   int* comb_row = reinterpret_cast<int*>(ws + L.comb_row);
@@ -82,12 +92,72 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     tile_start[b] = excl;
     excl += (lens[b] + kPage - 1) / kPage;
   }
+  // Row costs for the partition: a row with pages costs its pages plus
+  // kSegCost pages' worth for its segment start (query load, output write,
+  // pipeline refill), measured at about five pages on GB300.
+  int local_ne = 0;
+  for (int b = lo; b < hi; ++b) local_ne += lens[b] > 0 ? 1 : 0;
+  int ne_total = 0;
+  int ne_excl = block_exclusive_scan(local_ne, s_warp, &ne_total);
+  for (int b = lo; b < hi; ++b) {
+    row_cost[b] = tile_start[b] + kSegCost * ne_excl;
+    ne_excl += lens[b] > 0 ? 1 : 0;
+  }
   if (tid == 0) {
     tile_start[batch] = total;
+    row_cost[batch] = total + kSegCost * ne_total;
     s_chunk = total > 0 ? (total + pairs_per_group - 1) / pairs_per_group : 1;
   }
   __syncthreads();
   const int chunk = s_chunk;
+
+  // Pair p starts where the cumulative cost reaches p/ppg of the total: in
+  // the row whose cost range holds that point, past the row's start cost.
+  const long long cost_total = static_cast<long long>(total) + static_cast<long long>(kSegCost) * ne_total;
+  for (int pp = tid; pp <= pairs_per_group; pp += blockDim.x) {
+    int x = pp == 0 ? 0 : total;
+    if (pp > 0 && pp < pairs_per_group) {
+      const long long target = cost_total * pp / pairs_per_group;
+      int l = 0, r = batch - 1;            // largest row with row_cost <= target
+      while (l < r) {
+        const int mid = (l + r + 1) >> 1;
+        if (row_cost[mid] <= target) l = mid; else r = mid - 1;
+      }
+      const int n = tile_start[l + 1] - tile_start[l];
+      const long long off = target - row_cost[l] - (n > 0 ? kSegCost : 0);
+      x = tile_start[l] + static_cast<int>(off < 0 ? 0 : (off > n ? n : off));
+    }
+    pair_lo[pp] = x;
+  }
+  __syncthreads();
+  // pair_rank[p]: pairs before p that have pages.  A pair range can be empty
+  // (its cost share falls inside a row's start cost); a split row's parts
+  // are the non-empty pairs over it, numbered by rank.
+  if (tid < 32) {
+    int carry = 0;
+    for (int base = 0; base <= pairs_per_group; base += 32) {
+      const int pp = base + tid;
+      const int ne = pp < pairs_per_group && pair_lo[pp + 1] > pair_lo[pp] ? 1 : 0;
+      int x = ne;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (tid >= o) x += y;
+      }
+      if (pp <= pairs_per_group) pair_rank[pp] = carry + x - ne;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  __syncthreads();
+  // the pair whose page range [pair_lo[p], pair_lo[p+1]) holds page t
+  auto pair_of = [&](int t) {
+    int l = 0, r = pairs_per_group - 1;
+    while (l < r) {
+      const int mid = (l + r + 1) >> 1;
+      if (pair_lo[mid] <= t) l = mid; else r = mid - 1;
+    }
+    return l;
+  };
 
   // pass 2: pairs covering each row; slots for rows that are split
   local = 0;
@@ -96,8 +166,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     const int n = (lens[b] + kPage - 1) / kPage;
     int parts = 0, fp = 0;
     if (n > 0) {
-      fp = tile_start[b] / chunk;
-      parts = (tile_start[b] + n - 1) / chunk - fp + 1;
+      fp = pair_of(tile_start[b]);
+      parts = pair_rank[pair_of(tile_start[b] + n - 1) + 1] - pair_rank[fp];
     }
     first_pair[b] = fp;
     local += parts > 1 ? parts : 0;
@@ -110,7 +180,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   for (int b = lo; b < hi; ++b) {
     const int n = (lens[b] + kPage - 1) / kPage;
     int parts = 0;
-    if (n > 0) parts = (tile_start[b] + n - 1) / chunk - first_pair[b] + 1;
+    if (n > 0) parts = pair_rank[pair_of(tile_start[b] + n - 1) + 1] - pair_rank[first_pair[b]];
     slot_base[b] = parts > 1 ? slot_excl : -1;
     if (parts != 1) {
       for (int i = 0; i < sq; ++i) {
