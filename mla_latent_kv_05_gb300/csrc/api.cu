@@ -127,9 +127,9 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
 // Library-owned scratch of mla_decode_bf16_noalloc: the plan header, the
 // split-KV plan and the fp32 partial outputs, for callers that cannot hand
 // the library device memory.  40 MiB holds the partials of 76 CTA pairs (the
-// 152 SMs of a GB300: 152 slots x 128 heads x 512 x 4 B = 38 MiB) plus the
-// plan of up to kStaticMaxRows query rows.  One copy per device, shared by
-// every call on that device.
+// 152 SMs of a GB300: 152 slots x 128 heads x 512 bf16 = 19 MiB) plus the
+// plan of up to kStaticMaxRows query rows, with room to spare.  One copy per
+// device, shared by every call on that device.
 constexpr size_t kStaticScratchBytes = size_t{40} << 20;
 constexpr int kStaticMaxRows = 8192;
 constexpr int kStaticMaxDevices = 64;
