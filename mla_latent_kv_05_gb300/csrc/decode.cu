@@ -65,59 +65,63 @@ constexpr uint32_t kKSlot = 4 * 9 * kAtom;             // half page, nine chunks
 constexpr uint32_t kKGroup = 9 * kAtom;                // row-group stride of a K slot
 constexpr uint32_t kVSlot = 4 * 8 * kAtom;             // half page, eight latent chunks (32 KiB)
 constexpr uint32_t kVGroup = 8 * kAtom;                // row-group stride of a V slot
-constexpr uint32_t kRopeSlot = 4 * kAtom;               // half page, RoPE chunk only (FP8 score SM, 4 KiB)
 constexpr uint32_t kPChunk = 128 * 128;                // 64 tokens of P for 128 heads (16 KiB)
 constexpr int kPSlots = 2;
 constexpr int kMailSlots = 2;
 constexpr int kHalf = kPage / 2;                        // tokens per half page
 constexpr uint32_t kRawBytes = kHalf * kFp8Row;         // raw FP8 half page: 19,008 B
-constexpr int kMaxVSlots = 6, kMaxRaw = 4, kMaxLat = 4;
+constexpr int kMaxVSlots = 5, kMaxRaw = 4;
 
 // Shared-memory plans (bytes).  The small common region (alpha, 1/l, flags,
 // barriers) sits at the same offset in both ranks so remote stores and
 // arrivals can address it.
 //   bf16: rank 1 = 6 K slots (two 3-slot tiles); rank 0 = 5 V slots + 2 P
 //         slots of two chunks (96 tokens).
-//   FP8:  rank 1 dequantises every token once: 4 latent slots laid out
-//         exactly like V slots + 4 RoPE slots (two 2-half-page tiles) + 4 raw
-//         half pages; each finished latent slot is bulk-copied into one of
-//         rank 0's 6 V slots.  Rank 0 = 6 V slots + 2 one-chunk P slots.
+//   FP8:  each SM bulk-loads every raw half page (the second read is an L2
+//         hit) and dequantises what its own MMAs read: rank 1 = 4 K slots
+//         (two 2-slot tiles) + 4 raw half pages; rank 0 = 4 V slots + 2
+//         one-chunk P slots + 3 raw half pages.  Moving dequantised rows
+//         between the two SMs instead would cost more: shared-to-shared
+//         traffic inside a cluster runs at about 42 GB/s per pair on GB300.
 template <int kMode> struct Cfg;
 template <> struct Cfg<0> {
   static constexpr int kTileHalves = 3;
   static constexpr int kVSlots = 5;
-  static constexpr int kRaw1 = 0;
   static constexpr uint32_t kPSlotBytes = 2 * kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;
-  static constexpr uint32_t kOffRope = 0, kOffRaw1 = 0;
+  static constexpr int kRaw0 = 0, kRaw1 = 0;
+  static constexpr uint32_t kOffRaw0 = 0, kOffRaw1 = 0;
   static constexpr uint32_t kEnd1 = 2 * kTileHalves * kKSlot;
   static constexpr uint32_t kEnd0 = kOffP + kPSlots * kPSlotBytes;
   static constexpr uint32_t kOffMisc = kEnd1 > kEnd0 ? kEnd1 : kEnd0;
   static constexpr int kThreads = 384;
   static constexpr int kSmGroups = 2;          // softmax warp groups (4 warps each)
-  static constexpr int kDqWarp0 = 0, kDqWarps = 0;
+  static constexpr int kDqWarps1 = 0, kDqWarps0 = 0;
+  static constexpr int kEpWarps = 8;           // epilogue warps on rank 0 (256 columns each)
 };
 template <> struct Cfg<1> {
   static constexpr int kTileHalves = 2;
-  static constexpr int kVSlots = 6;
-  static constexpr int kRaw1 = 4;
+  static constexpr int kVSlots = 4;
   static constexpr uint32_t kPSlotBytes = kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;                       // rank 0
-  static constexpr uint32_t kOffRope = 2 * kTileHalves * kVSlot;            // rank 1: after the latent slots
-  static constexpr uint32_t kOffRaw1 = kOffRope + 2 * kTileHalves * kRopeSlot;
+  static constexpr int kRaw0 = 3, kRaw1 = 4;
+  static constexpr uint32_t kOffRaw0 = kOffP + kPSlots * kPSlotBytes;       // rank 0
+  static constexpr uint32_t kOffRaw1 = 2 * kTileHalves * kKSlot;            // rank 1: after the K slots
   static constexpr uint32_t kEnd1 = kOffRaw1 + kRaw1 * kRawBytes;
-  static constexpr uint32_t kEnd0 = kOffP + kPSlots * kPSlotBytes;
+  static constexpr uint32_t kEnd0 = kOffRaw0 + kRaw0 * kRawBytes;
   static constexpr uint32_t kOffMisc = ((kEnd1 > kEnd0 ? kEnd1 : kEnd0) + 1023) & ~1023u;
   static constexpr int kThreads = 512;
   static constexpr int kSmGroups = 1;          // 64-token tiles: one group of 4 warps takes all columns
-  static constexpr int kDqWarp0 = 8, kDqWarps = 8;
+  static constexpr int kDqWarps1 = 9;          // rank 1: warps 8..15 and 2, one value-group pair of 18 each
+  static constexpr int kDqWarps0 = 8;          // rank 0: warps 8..15, one latent value-group pair of 16 each
+  static constexpr int kEpWarps = 4;           // rank 0: four epilogue warps (512 columns each)
 };
 constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
 constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
 constexpr uint32_t kMiscMail = 1024;     // rank 0: fp32 1/l [2][128]
 constexpr uint32_t kMiscReq = 2048;      // rank 0: P slot of a rescale request
 constexpr uint32_t kMiscRawFlag = 2064;  // per raw stage: 1 = write zeros (bad page)
-constexpr uint32_t kMiscBar = 2080;
+constexpr uint32_t kMiscBar = kMiscRawFlag + 4 * kMaxRaw;
 enum Bar {
   KFULL = 0, KEMPTY = KFULL + 2,
   VFULL = KEMPTY + 2, VEMPTY = VFULL + kMaxVSlots,
@@ -126,16 +130,16 @@ enum Bar {
   QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY, LSUM,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
   RAWFULL = MBEMPTY + kMailSlots, RAWEMPTY = RAWFULL + kMaxRaw,
-  LDONE = RAWEMPTY + kMaxRaw,              // FP8 rank 1: latent slot dequantised (8 warps)
-  NBAR = LDONE + kMaxLat
+  NBAR = RAWEMPTY + kMaxRaw
 };
 constexpr uint32_t kMiscTmem = kMiscBar + NBAR * 8;
 constexpr uint32_t kMiscBytes = kMiscTmem + 16;
 template <int kMode> constexpr uint32_t smem_bytes() { return Cfg<kMode>::kOffMisc + kMiscBytes; }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory budget");
 static_assert(Cfg<0>::kVSlots <= kMaxVSlots && Cfg<1>::kVSlots <= kMaxVSlots, "V slot barriers");
-static_assert(Cfg<1>::kRaw1 <= kMaxRaw, "raw barriers");
-static_assert(2 * Cfg<1>::kTileHalves <= kMaxLat, "latent slot barriers");
+static_assert(Cfg<1>::kRaw1 <= kMaxRaw && Cfg<1>::kRaw0 <= kMaxRaw, "raw barriers");
+static_assert(Cfg<1>::kOffMisc % 1024 == 0 && Cfg<1>::kOffRaw0 % 16 == 0 && Cfg<1>::kOffRaw1 % 16 == 0,
+              "slot alignment");
 static_assert(Cfg<0>::kOffMisc % 1024 == 0, "slot alignment");
 
 // TMEM columns.
@@ -220,12 +224,16 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
 }
 
 // 32 e4m3 codes (8 words, lowest byte first) with their e8m0 scale byte ->
-// 16 bf16x2 words.  e4m3 -> f16 is exact in hardware, the product with the
-// power-of-two scale is exact in fp32 (no flush), and the result has at most
-// 4 significant bits, so the bf16 rounding is exact too.  NaN codes and the
-// NaN scale (0xFF) give NaN, as in the format definitions.
+// 16 bf16x2 words.  e4m3 -> f16 is exact in hardware and the product with
+// the power-of-two scale is exact in fp32 (no flush).  The product has at
+// most 4 significant bits, and for scale exponents e >= 3 its smallest bit is
+// at least 2^-133, the last bit of a bf16 subnormal, so the bf16 value is the
+// fp32 value's upper 16 bits: a byte permute, not a rounding conversion.
+// Below that (results under 2^-133) the rounding conversion is used.  NaN
+// codes and the NaN scale (0xFF) give NaN, as in the format definitions.
 __device__ __forceinline__ void dequant32(const uint32_t* wd, uint32_t e, uint32_t* o) {
   const float sc = __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : (e << 23)));
+  const bool trunc_exact = e >= 3;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     uint32_t h01, h23;
@@ -233,8 +241,14 @@ __device__ __forceinline__ void dequant32(const uint32_t* wd, uint32_t e, uint32
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<unsigned short>(wd[i] >> 16)));
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    o[2 * i] = pack_bf16x2(f01.x * sc, f01.y * sc);
-    o[2 * i + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
+    const float a = f01.x * sc, b = f01.y * sc, c = f23.x * sc, d = f23.y * sc;
+    if (trunc_exact) {
+      o[2 * i] = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
+      o[2 * i + 1] = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x7632);
+    } else {
+      o[2 * i] = pack_bf16x2(a, b);
+      o[2 * i + 1] = pack_bf16x2(c, d);
+    }
   }
 }
 
@@ -330,33 +344,32 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
 
   const bool smem_ok = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
-    // K tiles: the TMA bytes (bf16), or (FP8) the dequant warps plus rank 0's
-    // acknowledgement that the tile's latent copies have landed -- the
-    // buffer is rewritten only after the tile's S, so after those copies
+    // FP8: this SM's dequant warps
+    const uint32_t dq = static_cast<uint32_t>(rank == 1 ? C::kDqWarps1 : C::kDqWarps0);
+    constexpr uint32_t kEp = static_cast<uint32_t>(C::kEpWarps);
+    // K tiles: the TMA bytes (bf16) or the dequant warps (FP8)
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : static_cast<uint32_t>(C::kDqWarps + 1));
+      ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : dq);
       ptx::mbar_init(BAR(KEMPTY + s), 1);
     }
-    // V slots: the TMA bytes (bf16) or the bulk copy from rank 1 (FP8), each
-    // announced by one arrive with its byte count
+    // V slots: the TMA bytes (bf16) or the dequant warps (FP8)
     for (int s = 0; s < kMaxVSlots; ++s) {
-      ptx::mbar_init(BAR(VFULL + s), 1);
+      ptx::mbar_init(BAR(VFULL + s), kMode == 0 ? 1u : dq);
       ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
     for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128 * kSG); }
     ptx::mbar_init(BAR(QREADY), 128 * kSG);
     ptx::mbar_init(BAR(REQ), 2);
-    ptx::mbar_init(BAR(CORR), 8);
+    ptx::mbar_init(BAR(CORR), kEp);
     ptx::mbar_init(BAR(OFULL), 1);
-    ptx::mbar_init(BAR(OEMPTY), 256);
+    ptx::mbar_init(BAR(OEMPTY), 32 * kEp);
     ptx::mbar_init(BAR(LSUM), 128);
-    for (int s = 0; s < kMailSlots; ++s) { ptx::mbar_init(BAR(MBFULL + s), 128); ptx::mbar_init(BAR(MBEMPTY + s), 8); }
+    for (int s = 0; s < kMailSlots; ++s) { ptx::mbar_init(BAR(MBFULL + s), 128); ptx::mbar_init(BAR(MBEMPTY + s), kEp); }
     for (int s = 0; s < kMaxRaw; ++s) {
       ptx::mbar_init(BAR(RAWFULL + s), 1);
-      ptx::mbar_init(BAR(RAWEMPTY + s), kMode == 0 ? 1u : static_cast<uint32_t>(C::kDqWarps));
+      ptx::mbar_init(BAR(RAWEMPTY + s), kMode == 0 ? 1u : dq);
     }
-    for (int s = 0; s < kMaxLat; ++s) ptx::mbar_init(BAR(LDONE + s), kMode == 0 ? 1u : static_cast<uint32_t>(C::kDqWarps));
     ptx::fence_barrier_init();
   }
   if (warp == 2) {
@@ -394,10 +407,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
       int vs = 0; uint32_t vphase = 0;      // rank 0: V slot
       int rs = 0; uint32_t rphase = 0;      // FP8: raw ring
-      const int n_raw = C::kRaw1;
-      const uint32_t raw_off = C::kOffRaw1;
+      const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
+      const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
       volatile uint32_t* raw_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffRawFlag);
-      bool ok = kMode == 0 || rank == 1;    // FP8: rank 0 receives its V from rank 1
+      bool ok = true;
       while (ok && w.next(sg)) {
         const int hp_end = 2 * sg.t1;
         // Block-table entries are read one tile ahead, so their global-memory
@@ -482,123 +495,66 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
       }
     }
-  } else if (kMode == 1 && active && rank == 1 && warp >= C::kDqWarp0) {
-    // ------------------------------------------------------------ FP8 dequant (rank 1, warps 8..15)
-    // raw half page -> latent slot (16 value groups, laid out like a value-SM
-    // V slot) + RoPE slot (2 groups).  Lane = token, so the 32 lanes' 16-byte
-    // stores of one value group hit 32 different swizzled rows
-    // (conflict-free per 8 rows); warp wq of 8 takes value groups wq, wq+8
-    // and (wq < 2) wq+16 in one pass of independent chains.
-    constexpr int kDW = C::kDqWarps;
-    const int wq = warp - C::kDqWarp0;
+  } else if (kMode == 1 && active && (warp >= 8 || (warp == 2 && rank == 1))) {
+    // ------------------------------------------------------------ FP8 dequant
+    // raw half page -> rank 1: K slot (all 18 value groups, nine-chunk
+    // layout); rank 0: V slot (the 16 latent groups).  Warp wq takes value
+    // groups 2wq and 2wq+1; lane = (token lane % 16 and the same token + 16,
+    // group 2wq + lane / 16): two independent chains per lane, and each
+    // 8-lane phase of a 16-byte store hits eight different swizzled rows.
+    const int wq = warp == 2 ? 8 : warp - 8;
+    const int t = lane & 15, g = 2 * wq + (lane >> 4);
     const volatile uint32_t* raw_flag = reinterpret_cast<const volatile uint32_t*>(smem + kOffRawFlag);
-    auto store = [&](uint8_t* lat, uint8_t* rope, int g, const uint32_t* o) {
-      if (g < 16) store_group(lat, kVGroup, lane, g, o);
-      else store_group(rope, kAtom, lane, g - 16, o);
-    };
+    const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
+    const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
-    int kb = 0; uint32_t kphase = 0;
+    int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
+    int vs = 0; uint32_t vphase = 0;      // rank 0: V slot
     int rs = 0; uint32_t rphase = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
       const int hp_end = 2 * sg.t1;
       for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
         const int nh = min(TH, hp_end - h0);
-        // the tile buffer is free once S of the tile two back is done (its
-        // latent copies to rank 0 had landed before that S could start)
-        if (!wait_warp<true>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+        // rank 1: the tile's slots are free once S of the tile two back is done
+        if (rank == 1 && !wait_warp<false>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
         for (int j = 0; j < nh; ++j) {
-          const int ls = kb * TH + j;
-          uint8_t* lat = smem + static_cast<uint32_t>(ls) * kVSlot;
-          uint8_t* rope = smem + C::kOffRope + static_cast<uint32_t>(ls) * kRopeSlot;
+          // rank 0: the V slot is free once its P.V is done
+          if (rank == 0 && !wait_warp<false>(BAR(VEMPTY + vs), vphase ^ 1u, hdr)) { ok = false; break; }
           if (!wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
-          const bool zero = raw_flag[rs] != 0;
-          const uint8_t* row = smem + C::kOffRaw1 + static_cast<uint32_t>(rs) * kRawBytes + lane * kFp8Row;
-          // passes of up to three independent value groups: wq, wq+kDW, wq+2kDW, ...
-          for (int ga = wq; ga < kRow / 32; ga += 3 * kDW) {
-            const int gb = ga + kDW, gc = ga + 2 * kDW;
-            const bool hb = gb < kRow / 32, hc = gc < kRow / 32;
-            uint32_t o0[16], o1[16], o2[16];
-            if (!zero) {
-              dequant_group(row, ga, o0);
-              if (hb) dequant_group(row, gb, o1);
-              if (hc) dequant_group(row, gc, o2);
-            } else {
+          uint32_t o0[16], o1[16];
+          if (raw_flag[rs] == 0) {
+            const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + t * kFp8Row;
+            dequant_group(row, g, o0);
+            dequant_group(row + 16 * kFp8Row, g, o1);
+          } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) { o0[i] = 0u; o1[i] = 0u; o2[i] = 0u; }
-            }
-            store(lat, rope, ga, o0);
-            if (hb) store(lat, rope, gb, o1);
-            if (hc) store(lat, rope, gc, o2);
+            for (int e = 0; e < 16; ++e) { o0[e] = 0u; o1[e] = 0u; }
           }
-          ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA and the bulk copy
+          if (rank == 1) {
+            uint8_t* slot = smem + static_cast<uint32_t>(kb * TH + j) * kKSlot;
+            store_group(slot, kKGroup, t, g, o0);
+            store_group(slot, kKGroup, t + 16, g, o1);
+          } else {
+            uint8_t* slot = smem + static_cast<uint32_t>(vs) * kVSlot;
+            store_group(slot, kVGroup, t, g, o0);
+            store_group(slot, kVGroup, t + 16, g, o1);
+          }
+          ptx::fence_proxy_async_cta();      // generic smem writes -> visible to the MMA
           __syncwarp();
           if (lane == 0) {
             ptx::mbar_arrive(BAR(RAWEMPTY + rs));
-            ptx::mbar_arrive(BAR(LDONE + ls));
+            if (rank == 0) ptx::mbar_arrive(BAR(VFULL + vs));
           }
-          if (++rs == C::kRaw1) { rs = 0; rphase ^= 1u; }
+          if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
+          if (rank == 0 && ++vs == kVSlots) { vs = 0; vphase ^= 1u; }
         }
         if (!ok) break;
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(BAR(KFULL + kb));
+        if (rank == 1 && lane == 0) ptx::mbar_arrive(BAR(KFULL + kb));
         kb ^= 1;
         if (kb == 0) kphase ^= 1u;
-      }
-    }
-  } else if (kMode == 1 && active && rank == 1 && warp == 3) {
-    // ------------------------------------------------------------ FP8 latent forwarder (rank 1)
-    // Each dequantised latent slot goes to the next V slot of rank 0 in one
-    // shared-to-shared bulk copy, counted on that slot's VFULL barrier.
-    if (lane == 0) {
-      SegWalker w; w.init(tile_start, p.batch, lo, hi);
-      Segment sg;
-      int kb = 0; uint32_t kphase = 0;
-      int vs = 0; uint32_t vphase = 0;
-      bool ok = true;
-      while (ok && w.next(sg)) {
-        const int hp_end = 2 * sg.t1;
-        for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
-          const int nh = min(TH, hp_end - h0);
-          for (int j = 0; j < nh; ++j) {
-            const int ls = kb * TH + j;
-            if (!wait_bounded<false>(BAR(LDONE + ls), kphase, hdr) ||
-                !wait_bounded<true>(BAR(VEMPTY + vs), vphase ^ 1u, hdr)) { ok = false; break; }
-            const uint32_t vfull = ptx::mapa(BAR(VFULL + vs), 0);
-            ptx::mbar_arrive_expect_tx_remote(vfull, kVSlot);
-            ptx::bulk_copy_s2s(ptx::mapa(sbase + static_cast<uint32_t>(vs) * kVSlot, 0),
-                               sbase + static_cast<uint32_t>(ls) * kVSlot, kVSlot, vfull);
-            if (++vs == kVSlots) { vs = 0; vphase ^= 1u; }
-          }
-          kb ^= 1;
-          if (kb == 0) kphase ^= 1u;
-        }
-      }
-    }
-  } else if (kMode == 1 && active && rank == 0 && warp == 3) {
-    // ------------------------------------------------------------ FP8 copy acknowledger (rank 0)
-    // Once a tile's latent copies have landed, one arrive on rank 1's KFULL:
-    // the score SM then starts the tile, and its slots are rewritten only
-    // after that tile's S, so no copy is still reading them.
-    if (lane == 0) {
-      SegWalker w; w.init(tile_start, p.batch, lo, hi);
-      Segment sg;
-      int kb = 0;
-      int vs = 0; uint32_t vphase = 0;
-      bool ok = true;
-      while (ok && w.next(sg)) {
-        const int hp_end = 2 * sg.t1;
-        for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
-          const int nh = min(TH, hp_end - h0);
-          for (int j = 0; j < nh; ++j) {
-            if (!wait_bounded<false>(BAR(VFULL + vs), vphase, hdr)) { ok = false; break; }
-            if (++vs == kVSlots) { vs = 0; vphase ^= 1u; }
-          }
-          if (!ok) break;
-          ptx::mbar_arrive_remote(ptx::mapa(BAR(KFULL + kb), 1));
-          kb ^= 1;
-        }
       }
     }
   } else if (active && warp == 1 && rank == 1) {
@@ -622,15 +578,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t d = tmem + kSCol + static_cast<uint32_t>(kN * sb);
-          // bf16: nine chunks per row group in one slot run; FP8: the latent
-          // chunks in V-slot layout (8 KiB per row group) and the RoPE chunk
-          // in its own slots (1 KiB per row group)
-          const uint64_t desc0 =
-              kMode == 0 ? ptx::sdesc_sw128(sbase + static_cast<uint32_t>(kb * TH) * kKSlot, 16, kKGroup)
-                         : ptx::sdesc_sw128(sbase + static_cast<uint32_t>(kb * TH) * kVSlot, 16, kVGroup);
-          const uint64_t rope0 =
-              kMode == 0 ? desc0 + static_cast<uint64_t>((8 * kAtom) >> 4)
-                         : ptx::sdesc_sw128(sbase + C::kOffRope + static_cast<uint32_t>(kb * TH) * kRopeSlot, 16, kAtom);
+          // nine chunks per row group in one slot run (the RoPE chunk is the
+          // ninth, 8 KiB into each row group)
+          const uint64_t desc0 = ptx::sdesc_sw128(sbase + static_cast<uint32_t>(kb * TH) * kKSlot, 16, kKGroup);
+          const uint64_t rope0 = desc0 + static_cast<uint64_t>((8 * kAtom) >> 4);
 #pragma unroll
           for (int k = 0; k < kRow / 16; ++k) {
             const uint64_t bdesc = k < 32 ? desc0 + static_cast<uint64_t>(((k >> 2) * kAtom + (k & 3) * 32) >> 4)
@@ -714,9 +665,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                 ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, (h0 > 2 * sg.t0 || k > 0) ? 1u : 0u);
               }
             }
-            // FP8: rank 1's forwarder waits for free V slots too
-            if constexpr (kMode == 0) ptx::mma_commit(BAR(VEMPTY + vs));
-            else ptx::mma_commit_mc(BAR(VEMPTY + vs), static_cast<uint16_t>(3u));
+            ptx::mma_commit(BAR(VEMPTY + vs));
           }
           __syncwarp();
           if (++vs == kVSlots) { vs = 0; vphase ^= 1u; }
@@ -904,12 +853,13 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         if (++ms == kMailSlots) { ms = 0; mphase ^= 1u; }
       }
     }
-  } else if (active && warp >= 4 && warp < 12 && rank == 0) {
+  } else if (active && warp >= 4 && warp < 4 + C::kEpWarps && rank == 0) {
     // ------------------------------------------------------------ rescale + epilogue
-    // Eight warps: warps 4..7 take latent columns [0, 256) of head rows
-    // 0..127, warps 8..11 columns [256, 512).
+    // bf16: eight warps, warps 4..7 take latent columns [0, 256) of head rows
+    // 0..127, warps 8..11 columns [256, 512).  FP8: warps 4..7 take all 512.
+    constexpr int kEpChunks = 16 / (C::kEpWarps / 4);   // 32-column chunks per warp
     const int h = (threadIdx.x - 128) & 127;
-    const int c0 = 8 * ((warp - 4) >> 2);     // first 32-column chunk of this warp
+    const int c0 = kEpChunks * ((warp - 4) >> 2);     // first 32-column chunk of this warp
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
@@ -935,7 +885,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           const float a = alpha_buf[*req_slot * 128 + h];
           if (__any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
-            for (int cc = c0; cc < c0 + 8; ++cc) {
+            for (int cc = c0; cc < c0 + kEpChunks; ++cc) {
               uint32_t r[32];
               ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
               ptx::tmem_wait_ld();
@@ -976,7 +926,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           split ? part_out + (static_cast<size_t>(group * spq + slot_base[sg.b] + (pair_rank[pl] - pair_rank[first_pair[sg.b]])) * kHeads + h) * kDc
                 : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
 #pragma unroll 1
-      for (int cc = c0; cc < c0 + 8; ++cc) {
+      for (int cc = c0; cc < c0 + kEpChunks; ++cc) {
         uint32_t r[32];
         ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
         ptx::tmem_wait_ld();

@@ -216,6 +216,35 @@ def test_fp8_single_token_is_bit_exact_dequant(cuda_device):
         assert torch.equal(got, want.expand(128, 512)), b
 
 
+def test_fp8_every_token_position_is_bit_exact_dequant(cuda_device):
+    # Batch row b attends to token b of its page and to nothing else: only
+    # the first RoPE dimension of the query is set, and token b's first RoPE
+    # value is +448 against -448 for every other token, so every other
+    # weight is exp(-4000) = 0 and out = token b's dequantised latent,
+    # exactly.  All 64 positions of a page are covered, which includes the
+    # rows each SM of the pair dequantises.
+    n = 64
+    inp = gen.make_inputs(n, 1, [n] * n, kv_dtype="fp8", seed=33)
+    inp.q_absorbed.zero_()
+    inp.q_rope.zero_()
+    inp.q_rope[..., 0] = 64.0
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        rows = inp.kv_cache[page]
+        rows[:, 512:576] = 0                 # RoPE codes: zero ...
+        rows[:, 576 + 16] = 127              # ... with scale 1 on the first RoPE group
+        rows[:, 512] = 0xFE                  # -448 for every token
+        rows[b, 512] = 0x7E                  # +448 for token b
+        rows[b, :8] = torch.tensor([0x00, 0x80, 0x01, 0x81, 0x7E, 0xFE, 0x08, 0x77], dtype=torch.uint8)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        want = _dequant_bf16(inp.kv_cache[page, b])[:512]
+        got = out[b, 0].cpu()
+        assert torch.equal(got, want.expand(128, 512)), b   # value-exact (-0 == +0)
+
+
 @pytest.mark.parametrize("lens", [[1, 63, 64, 65, 200], [3000, 17]])
 def test_fp8_ragged(cuda_device, lens):
     inp = gen.make_inputs(len(lens), 1, lens, kv_dtype="fp8", seed=7 + len(lens))
