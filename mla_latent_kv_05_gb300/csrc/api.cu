@@ -85,9 +85,11 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   const WsLayout L = ws_layout(batch, sq, pairs);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  CUtensorMap tmap_k, tmap_v;    // half pages: 9 chunks (score SM), 8 latent chunks (value SM)
+  // half pages: chunks 0..4 and 5..8 (score SM), the 8 latent chunks (value SM)
+  CUtensorMap tmap_k, tmap_kb, tmap_v;
   if (!fp8) {
-    st = make_cache_tmap(&tmap_k, kv_cache, num_pages, 9);
+    st = make_cache_tmap(&tmap_k, kv_cache, num_pages, 5);
+    if (st == MLA_OK) st = make_cache_tmap(&tmap_kb, kv_cache, num_pages, 4);
     if (st == MLA_OK) st = make_cache_tmap(&tmap_v, kv_cache, num_pages, 8);
     if (st != MLA_OK) return st;
   }
@@ -117,7 +119,7 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   const bool pdl = ev0 == nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
   const cudaError_t le = fp8 ? launch_decode_fp8(p, ppg * sq, pdl, stream)
-                             : launch_decode_bf16(tmap_k, tmap_v, p, ppg * sq, pdl, stream);
+                             : launch_decode_bf16(tmap_k, tmap_kb, tmap_v, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;

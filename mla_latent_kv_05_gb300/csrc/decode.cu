@@ -63,6 +63,8 @@ namespace dk {
 constexpr uint32_t kAtom = 1024;                        // 8 rows x 128 B, 128B swizzle
 constexpr uint32_t kKSlot = 4 * 9 * kAtom;             // half page, nine chunks (36 KiB)
 constexpr uint32_t kKGroup = 9 * kAtom;                // row-group stride of a K slot
+constexpr uint32_t kKA = 4 * 5 * kAtom;                // bf16 score SM: half page, chunks 0..4 (20 KiB)
+constexpr uint32_t kKB = 4 * 4 * kAtom;                // bf16 score SM: half page, chunks 5..8 (16 KiB)
 constexpr uint32_t kVSlot = 4 * 8 * kAtom;             // half page, eight latent chunks (32 KiB)
 constexpr uint32_t kVGroup = 8 * kAtom;                // row-group stride of a V slot
 constexpr uint32_t kPChunk = 128 * 128;                // 64 tokens of P for 128 heads (16 KiB)
@@ -124,7 +126,8 @@ constexpr uint32_t kMiscRawFlag = 2064;  // per raw stage: 1 = write zeros (bad 
 constexpr uint32_t kMiscBar = kMiscRawFlag + 4 * kMaxRaw;
 enum Bar {
   KFULL = 0, KEMPTY = KFULL + 2,
-  VFULL = KEMPTY + 2, VEMPTY = VFULL + kMaxVSlots,
+  KFULLB = KEMPTY + 2, KEMPTYB = KFULLB + 2,   // bf16 score SM: the chunk 5..8 part of a tile
+  VFULL = KEMPTYB + 2, VEMPTY = VFULL + kMaxVSlots,
   PFULL = VEMPTY + kMaxVSlots, PEMPTY = PFULL + kPSlots,
   SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + 2,
   QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY, LSUM,
@@ -306,8 +309,8 @@ __device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* 
 
 template <int kMode>   // 0: bf16 cache via TMA, 1: FP8 cache via bulk copies + dequant
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dk::Cfg<kMode>::kThreads, 1)
-mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                       const DecodeParams p) {
+mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_kb,
+                       const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using namespace dk;
   using C = Cfg<kMode>;
   constexpr int TH = C::kTileHalves;            // half pages per tile
@@ -351,6 +354,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : dq);
       ptx::mbar_init(BAR(KEMPTY + s), 1);
+      ptx::mbar_init(BAR(KFULLB + s), 1);
+      ptx::mbar_init(BAR(KEMPTYB + s), 1);
     }
     // V slots: the TMA bytes (bf16) or the dequant warps (FP8)
     for (int s = 0; s < kMaxVSlots; ++s) {
@@ -376,7 +381,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     ptx::tmem_alloc(sbase + kOffTmemPtr, kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (kMode == 0 && warp == 0 && lane == 0) ptx::prefetch_tmap(rank == 1 ? &tmap_k : &tmap_v);
+  if (kMode == 0 && warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(rank == 1 ? &tmap_k : &tmap_v);
+    if (rank == 1) ptx::prefetch_tmap(&tmap_kb);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -431,16 +439,32 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           if constexpr (kMode == 0) {
             // a bad page is read fully outside the tensor, which fills zeros
             if (rank == 1) {
+              // A tile buffer holds the tile's chunks 0..4 (A part) and
+              // chunks 5..8 (B part) of every half page in two blocks.  S
+              // consumes the A part first, so the next tile's A part is
+              // refilled while S still reads the B part.
+              const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);
+              int wq[TH];
+#pragma unroll
+              for (int j = 0; j < TH; ++j) {
+                const int page = pages[j];
+                if (j < nh && page < 0) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
+                wq[j] = (page < 0 ? p.num_pages : page) * 8 + ((h0 + j) & 1) * 4;
+              }
               if (!wait_bounded<true>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
-              ptx::mbar_arrive_expect_tx(BAR(KFULL + kb), static_cast<uint32_t>(nh) * kKSlot);
+              ptx::mbar_arrive_expect_tx(BAR(KFULL + kb), static_cast<uint32_t>(nh) * kKA);
 #pragma unroll
               for (int j = 0; j < TH; ++j) {
                 if (j >= nh) break;
-                const int hp = h0 + j, page = pages[j];
-                if (page < 0) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
-                const int wq = (page < 0 ? p.num_pages : page) * 8 + (hp & 1) * 4;
-                ptx::tma_load_4d(sbase + static_cast<uint32_t>(kb * TH + j) * kKSlot, &tmap_k, BAR(KFULL + kb),
-                                 0, 0, 0, wq, pol);
+                ptx::tma_load_4d(tbase + static_cast<uint32_t>(j) * kKA, &tmap_k, BAR(KFULL + kb), 0, 0, 0, wq[j], pol);
+              }
+              if (!wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+              ptx::mbar_arrive_expect_tx(BAR(KFULLB + kb), static_cast<uint32_t>(nh) * kKB);
+#pragma unroll
+              for (int j = 0; j < TH; ++j) {
+                if (j >= nh) break;
+                ptx::tma_load_4d(tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(j) * kKB, &tmap_kb,
+                                 BAR(KFULLB + kb), 0, 0, 5, wq[j], pol);
               }
               kb ^= 1;
               if (kb == 0) kphase ^= 1u;
@@ -576,10 +600,35 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         if (!wait_warp<false>(BAR(KFULL + kb), kphase, hdr) ||
             !wait_warp<false>(BAR(SEMPTY + sb), sphase ^ 1u, hdr)) { ok = false; break; }
         ptx::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t d = tmem + kSCol + static_cast<uint32_t>(kN * sb);
-          // nine chunks per row group in one slot run (the RoPE chunk is the
-          // ninth, 8 KiB into each row group)
+        const uint32_t d = tmem + kSCol + static_cast<uint32_t>(kN * sb);
+        if constexpr (kMode == 0) {
+          // A part (K-steps 0..19, chunks 0..4, 5 KiB per row group), then
+          // B part (K-steps 20..35, chunks 5..8, 4 KiB per row group); the
+          // A part's slots are released as soon as its MMAs are done
+          const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);
+          if (lane == 0) {
+            const uint64_t da = ptx::sdesc_sw128(tbase, 16, 5 * kAtom);
+#pragma unroll
+            for (int k = 0; k < 20; ++k)
+              ptx::mma_ts(d, tmem + kQCol + 8u * k, da + static_cast<uint64_t>(((k >> 2) * kAtom + (k & 3) * 32) >> 4),
+                          kIdescS, k > 0 ? 1u : 0u);
+            ptx::mma_commit(BAR(KEMPTY + kb));
+          }
+          __syncwarp();
+          if (!wait_warp<false>(BAR(KFULLB + kb), kphase, hdr)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint64_t db = ptx::sdesc_sw128(tbase + static_cast<uint32_t>(TH) * kKA, 16, 4 * kAtom);
+#pragma unroll
+            for (int k = 20; k < kRow / 16; ++k)
+              ptx::mma_ts(d, tmem + kQCol + 8u * k,
+                          db + static_cast<uint64_t>((((k >> 2) - 5) * kAtom + (k & 3) * 32) >> 4), kIdescS, 1u);
+            ptx::mma_commit(BAR(KEMPTYB + kb));
+            ptx::mma_commit(BAR(SFULL + sb));
+          }
+        } else if (lane == 0) {
+          // FP8: nine chunks per row group in one slot run (the RoPE chunk is
+          // the ninth, 8 KiB into each row group)
           const uint64_t desc0 = ptx::sdesc_sw128(sbase + static_cast<uint32_t>(kb * TH) * kKSlot, 16, kKGroup);
           const uint64_t rope0 = desc0 + static_cast<uint64_t>((8 * kAtom) >> 4);
 #pragma unroll
@@ -958,8 +1007,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
 // (half-page boxes: nine chunks for rank 1, eight for rank 0); 1: FP8 cache
 // (p.kv_fp8; tensor maps unused).
 template <int kMode>
-cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
-                               int n_pairs, bool pdl, cudaStream_t stream) {
+cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
+                               const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
   auto kern = mla_decode_pair_kernel<kMode>;
   static int configured_device = -1;
   int dev = 0;
@@ -979,18 +1028,18 @@ cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tma
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmap_k, tmap_v, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmap_k, tmap_kb, tmap_v, p);
 }
 
-cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
-                               int n_pairs, bool pdl, cudaStream_t stream) {
-  return launch_decode_mode<0>(tmap_k, tmap_v, p, n_pairs, pdl, stream);
+cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
+                               const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
+  return launch_decode_mode<0>(tmap_k, tmap_kb, tmap_v, p, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return launch_decode_mode<1>(unused, unused, p, n_pairs, pdl, stream);
+  return launch_decode_mode<1>(unused, unused, unused, p, n_pairs, pdl, stream);
 }
 
 int decode_max_pairs() {

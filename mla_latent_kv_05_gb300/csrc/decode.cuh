@@ -24,8 +24,10 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_page
                         void* ws, const WsLayout& L, cudaStream_t stream);
 // pdl: launch as a programmatic dependent of the planner (the kernel waits on
 // griddepcontrol before reading the plan)
-cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeParams& p,
-                               int n_pairs, bool pdl, cudaStream_t stream);
+// tmap_k / tmap_kb: half-page boxes of chunks 0..4 / 5..8 (score SM);
+// tmap_v: half-page boxes of the eight latent chunks (value SM)
+cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
+                               const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 int decode_max_pairs();
 cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows, __nv_bfloat16* out, float* lse,
