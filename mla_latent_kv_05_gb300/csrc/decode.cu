@@ -383,7 +383,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   }
   if (kMode == 0 && warp == 0 && lane == 0) {
     ptx::prefetch_tmap(rank == 1 ? &tmap_k : &tmap_v);
-    if (rank == 1) ptx::prefetch_tmap(&tmap_kb);
+    ptx::prefetch_tmap(&tmap_kb);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -458,14 +458,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                 if (j >= nh) break;
                 ptx::tma_load_4d(tbase + static_cast<uint32_t>(j) * kKA, &tmap_k, BAR(KFULL + kb), 0, 0, 0, wq[j], pol);
               }
-              if (!wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
-              ptx::mbar_arrive_expect_tx(BAR(KFULLB + kb), static_cast<uint32_t>(nh) * kKB);
-#pragma unroll
-              for (int j = 0; j < TH; ++j) {
-                if (j >= nh) break;
-                ptx::tma_load_4d(tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(j) * kKB, &tmap_kb,
-                                 BAR(KFULLB + kb), 0, 0, 5, wq[j], pol);
-              }
+              // (the B parts are issued by rank 0: its TMA unit is less busy)
               kb ^= 1;
               if (kb == 0) kphase ^= 1u;
             } else {
@@ -581,6 +574,51 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         if (kb == 0) kphase ^= 1u;
       }
     }
+  } else if (kMode == 0 && active && warp == 3 && rank == 0) {
+    // ------------------------------------------------------------ B-part loader for rank 1 (bf16)
+    // The B part (chunks 5..8) of each of rank 1's K tiles, loaded by this
+    // CTA's TMA unit as a multicast whose only destination is rank 1: the
+    // data and the complete_tx land at the same offsets there.  Rank 1's S
+    // commits the release of a B part to this CTA (KEMPTYB).
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_normal();
+      SegWalker w; w.init(tile_start, p.batch, lo, hi);
+      Segment sg;
+      int kb = 0; uint32_t kphase = 0;
+      bool ok = true;
+      while (ok && w.next(sg)) {
+        const int hp_end = 2 * sg.t1;
+        int next_pages[TH];
+#pragma unroll
+        for (int j = 0; j < TH; ++j) next_pages[j] = 2 * sg.t0 + j < hp_end ? half_page(sg.b, 2 * sg.t0 + j) : 0;
+        for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
+          const int nh = min(TH, hp_end - h0);
+          int wq[TH];
+#pragma unroll
+          for (int j = 0; j < TH; ++j) {
+            wq[j] = (next_pages[j] < 0 ? p.num_pages : next_pages[j]) * 8 + ((h0 + j) & 1) * 4;
+            next_pages[j] = h0 + TH + j < hp_end ? half_page(sg.b, h0 + TH + j) : 0;
+          }
+          if (!wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx_remote(ptx::mapa(BAR(KFULLB + kb), 1), static_cast<uint32_t>(nh) * kKB);
+          const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);   // rank 1's tile buffer
+#pragma unroll
+          for (int j = 0; j < TH; ++j) {
+            if (j >= nh) break;
+            ptx::tma_load_4d_mc(tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(j) * kKB, &tmap_kb,
+                                BAR(KFULLB + kb), 0, 0, 5, wq[j], static_cast<uint16_t>(2u), pol);
+          }
+          kb ^= 1;
+          if (kb == 0) kphase ^= 1u;
+        }
+      }
+      // rank 1's last S commits arrive here: wait for them before this CTA may leave
+      for (int s = 0; s < 2 && ok; ++s) {
+        ok = wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr);
+        kb ^= 1;
+        if (kb == 0) kphase ^= 1u;
+      }
+    }
   } else if (active && warp == 1 && rank == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
     // One tile = TH adjacent half-page slots = one kN-row K-major operand
@@ -623,7 +661,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             for (int k = 20; k < kRow / 16; ++k)
               ptx::mma_ts(d, tmem + kQCol + 8u * k,
                           db + static_cast<uint64_t>((((k >> 2) - 5) * kAtom + (k & 3) * 32) >> 4), kIdescS, 1u);
-            ptx::mma_commit(BAR(KEMPTYB + kb));
+            ptx::mma_commit_mc(BAR(KEMPTYB + kb), static_cast<uint16_t>(1u));   // rank 0 issues the B loads
             ptx::mma_commit(BAR(SFULL + sb));
           }
         } else if (lane == 0) {

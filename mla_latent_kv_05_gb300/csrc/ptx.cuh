@@ -158,6 +158,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
                " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
                :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy) : "memory");
 }
+// Same, multicast: the box lands at offset `dst` of the shared memory of every
+// CTA in `mask` (this CTA need not be one of them), and each of them gets the
+// complete_tx on its barrier at offset `bar`.
+__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const void* tmap, uint32_t bar, int32_t x, int32_t y,
+                                               int32_t z, int32_t w, uint16_t mask, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+               ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;"
+               :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask), "l"(policy)
+               : "memory");
+}
 // 1-D bulk copy global -> shared (size and both addresses multiples of 16 B).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                           uint64_t policy) {
