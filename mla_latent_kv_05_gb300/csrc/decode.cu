@@ -28,22 +28,31 @@
 // with N = 64, so the score SM works on 96-token tiles (three half pages).
 // The cache is described to TMA as a 4-D tensor (64 columns, 8 rows, 9
 // column chunks, 8-row groups) with strides 1152 B (row), 128 B (chunk) and
-// 9216 B (row group); one box of 4 row groups is a half page (32 tokens,
-// 36 KiB with all nine chunks, 32 KiB with the eight latent chunks) and
-// lands as 8-row x 128-byte swizzle atoms ordered (row group, chunk, row).
-// Consecutive half-page slots therefore continue each other's row-group
-// sequence at a constant 9216-byte stride, so three adjacent slots are one
-// 96-row K-major operand, whatever pages they came from.  The value SM keeps
-// half-page V slots (atoms at 1 KiB per chunk, 8 KiB per row group), read as
-// MN-major operands 16 tokens at a time.  Both ranks read every half page;
-// the second read is an L2 hit.  The FP8 cache is bulk-copied as raw half
-// pages and dequantised by four warps into the same layouts (64-token tiles
-// there, as the raw buffers take the shared memory of the third slot).
+// 9216 B (row group); a box of 4 row groups is a half page and lands as
+// 8-row x 128-byte swizzle atoms ordered (row group, chunk, row).  A score
+// SM tile buffer holds two blocks: chunks 0..4 (A part) and chunks 5..8 (B
+// part) of its three half pages.  In each block consecutive slots continue
+// each other's row-group sequence at a constant stride (5 KiB, 4 KiB), so a
+// block is one 96-row K-major operand, whatever pages the slots came from.
+// S consumes the A part first and releases it, so the next tile's A part
+// loads while S reads the B part.  The A parts are loaded by the score SM,
+// the B parts by the value SM's TMA unit (multicast to the score SM alone),
+// because each TMA operation costs the issuing SM about 225 ns.  The value
+// SM keeps half-page V slots (atoms at 1 KiB per chunk, 8 KiB per row
+// group), read as MN-major operands 16 tokens at a time.  Both ranks read
+// every half page; the second read is an L2 hit.
+//
+// The FP8 cache is bulk-copied as raw half pages by both SMs, and each SM
+// dequantises what its own MMAs read (score SM: all nine chunks into the
+// nine-chunk K layout; value SM: the eight latent chunks into V slots), in
+// 64-token tiles (the raw buffers take the shared memory of a third slot).
+// Moving dequantised rows between the two SMs would cost more than the
+// second dequant: traffic inside a cluster runs at about 42 GB/s per pair.
 //
 // Lazy rescaling: rank 1 keeps a per-head reference max m_ref (raw score
 // units) and moves it only when a tile's max exceeds it by more than 16 in
-// log2 units, so P <= 2^16 and O is rescaled only on those tiles; eight
-// epilogue warps on rank 0 (256 columns each) do the rescale.
+// log2 units, so P <= 2^16 and O is rescaled only on those tiles; the
+// epilogue warps on rank 0 (eight for bf16, four for FP8) do the rescale.
 //
 // Every wait is bounded (wait_bounded / wait_warp); a timeout records
 // MLA_STATUS_TIMEOUT and raises an abort flag so every role leaves its loop
@@ -621,9 +630,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     }
   } else if (active && warp == 1 && rank == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
-    // One tile = TH adjacent half-page slots = one kN-row K-major operand
-    // (8-row atoms every kKGroup bytes); K-step k reads chunk k/4 at byte
-    // 32*(k%4) inside the atoms.
+    // One tile = TH adjacent half-page slots = one kN-row K-major operand;
+    // K-step k reads chunk k/4 at byte 32*(k%4) inside the 8-row atoms.
     SegWalker w; w.init(tile_start, p.batch, lo, hi);
     Segment sg;
     int kb = 0; uint32_t kphase = 0;
