@@ -53,12 +53,19 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources' code: line comments and blank lines are
+    dropped, so a comment-only edit keeps recorded counters valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_05_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                lines = []
+                for line in f:
+                    code = line.split("//", 1)[0].rstrip() if not line.lstrip().startswith("#include") else line.rstrip()
+                    if code.strip():
+                        lines.append(code)
+            h.update(name.encode() + "\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 
