@@ -105,6 +105,7 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   p.num_pages = num_pages;
   p.max_pages = max_pages;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.fp8_fallback = 0;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.ws = static_cast<uint8_t*>(workspace);

@@ -110,6 +110,7 @@ template <> struct Cfg<0> {
   static constexpr int kDqWarps1 = 0, kDqWarps0 = 0;
   static constexpr int kEpWarps = 8;           // epilogue warps on rank 0 (256 columns each)
 };
+// FP8 modes: 1 = exact bf16 operands; 2 = f16 operands (same layout)
 template <> struct Cfg<1> {
   static constexpr int kTileHalves = 2;
   static constexpr int kVSlots = 4;
@@ -127,6 +128,7 @@ template <> struct Cfg<1> {
   static constexpr int kDqWarps0 = 8;          // rank 0: warps 8..15, one latent value-group pair of 16 each
   static constexpr int kEpWarps = 4;           // rank 0: four epilogue warps (512 columns each)
 };
+template <> struct Cfg<2> : Cfg<1> {};
 constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
 constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
 constexpr uint32_t kMiscMail = 1024;     // rank 0: fp32 1/l [2][128]
@@ -159,10 +161,22 @@ constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
 constexpr uint32_t kSCol = 320;    // rank 1: two S buffers of N columns (N <= 96)
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 256, 0, 1);  // A = P (K-major), B = V (MN-major)
+// P.V: A = P (K-major), B = V (MN-major); bf16, or f16 in the FP8 f16 mode
+template <int kMode>
+constexpr uint32_t kIdescPV = kMode == 2 ? ptx::idesc_f16(128, 256, 0, 1) : ptx::idesc_bf16(128, 256, 0, 1);
 
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kRescaleThreshold = 16.0f;  // log2 units: P <= 2^16 (exact in relative terms; O stays far from fp32 overflow)
+// log2 units: P <= 2^16 (exact in relative terms; O stays far from fp32
+// overflow).  The FP8 f16 mode keeps P <= 2^15, inside the f16 range.
+template <int kMode>
+constexpr float kRescaleThreshold = kMode == 2 ? 15.0f : 16.0f;
+
+// FP8 f16 mode: a scale exponent e in [113, 134] makes every e4m3 code times
+// 2^(e-127) an exact f16 number (largest 448 * 2^7 = 57344 < 65504; smallest
+// step 2^-9 * 2^-14 = 2^-23, above the f16 subnormal step 2^-24), and keeps
+// the f16 scale itself normal.
+constexpr uint32_t kF16ScaleLo = 113, kF16ScaleHi = 134;
+constexpr float kF16Max = 65504.0f;
 
 struct Segment {
   int b;          // batch row
@@ -201,6 +215,12 @@ struct SegWalker {
     return false;
   }
 };
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -264,10 +284,31 @@ __device__ __forceinline__ void dequant32(const uint32_t* wd, uint32_t e, uint32
   }
 }
 
+// FP8 f16 mode: 32 e4m3 codes with their e8m0 scale byte -> 16 f16x2 words,
+// each the exact hardware e4m3 -> f16 conversion times the f16 scale 2^(e-127)
+// (a packed f16 multiply, exact for e in [kF16ScaleLo, kF16ScaleHi], where no
+// product leaves the f16 range).  Returns false (and writes nothing useful)
+// for a scale outside that range.
+__device__ __forceinline__ bool dequant32_f16(const uint32_t* wd, uint32_t e, uint32_t* o) {
+  const bool in_range = e >= kF16ScaleLo && e <= kF16ScaleHi;
+  const uint32_t sh = ((e - 112u) & 31u) << 10;
+  const uint32_t sc = sh | (sh << 16);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t h01, h23;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<unsigned short>(wd[i] & 0xFFFFu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<unsigned short>(wd[i] >> 16)));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i]) : "r"(h01), "r"(sc));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i + 1]) : "r"(h23), "r"(sc));
+  }
+  return in_range;
+}
+
 // Dequantise value group g (32 values) of raw FP8 row `row` (2-byte aligned
 // in shared memory) into 16 bf16x2 words.  The 32 codes are read as nine
 // aligned words and funnel-shifted by the row's misalignment (0 or 2 bytes).
-__device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint32_t* o) {
+template <bool kF16 = false>
+__device__ __forceinline__ bool dequant_group(const uint8_t* row, int g, uint32_t* o) {
   const uint8_t* src = row + 32 * g;
   const uintptr_t a = reinterpret_cast<uintptr_t>(src);
   const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
@@ -277,7 +318,12 @@ __device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint32_
   for (int i = 0; i < 9; ++i) u[i] = w[i];
 #pragma unroll
   for (int i = 0; i < 8; ++i) wd[i] = __funnelshift_r(u[i], u[i + 1], sh);
-  dequant32(wd, row[kRow + g], o);
+  if constexpr (kF16) {
+    return dequant32_f16(wd, row[kRow + g], o);
+  } else {
+    dequant32(wd, row[kRow + g], o);
+    return true;
+  }
 }
 
 // Store 16 bf16x2 words (32 values of value group g) as token r of a
@@ -297,8 +343,31 @@ __device__ __forceinline__ void store_group(uint8_t* slot, uint32_t group_stride
 // absorbed query at byte 128c, chunk 8: the RoPE query) with 32-byte loads
 // and store them into the TMEM lane row at column 32c (two bf16 per column).
 // Two chunks per round trip.
-template <int C0, int C1>
-__device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* qr, uint32_t taddr) {
+// bf16x2 word -> f16x2 word (round to nearest); qmax tracks the largest
+// magnitude seen, so that values past the f16 range can be detected.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float& qmax) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  qmax = max3(qmax, fabsf(lo), fabsf(hi));
+  return pack_f16x2(lo, hi);
+}
+
+// With kF16 (FP8 f16 mode) the query is stored as f16, and qmax returns its
+// largest magnitude.
+template <int C0, int C1, bool kF16 = false>
+__device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* qr, uint32_t taddr, float& qmax) {
+  if constexpr (kF16) {
+    // one chunk per round trip: the conversion needs the registers
+#pragma unroll 1
+    for (int c = C0; c < C1; ++c) {
+      uint32_t r0[32];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) ptx::ld_global_nc_v8((c < 8 ? qa + c * 128 : qr) + 32 * v, r0 + 8 * v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r0[i] = bf16x2_to_f16x2(r0[i], qmax);
+      ptx::tmem_st32(taddr + 32u * c, r0);
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c = C0; c < C1; c += 2) {
     uint32_t r0[32], r1[32];
@@ -316,7 +385,10 @@ __device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* 
 
 }  // namespace dk
 
-template <int kMode>   // 0: bf16 cache via TMA, 1: FP8 cache via bulk copies + dequant
+// kMode 0: bf16 cache via TMA; 1: FP8 cache via bulk copies + dequant to
+// bf16 operands; 2: FP8 cache with f16 operands (flags inputs outside the
+// f16-exact range, which mode 1 then recomputes)
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dk::Cfg<kMode>::kThreads, 1)
 mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_kb,
                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -327,7 +399,9 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   constexpr int kSG = C::kSmGroups;             // softmax warp groups
   constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
-  constexpr uint32_t kIdescS = ptx::idesc_bf16(128, kN, 0, 0);   // A = Q (TMEM), B = K (K-major)
+  constexpr bool kF16 = kMode == 2;               // FP8 with f16 operands
+  constexpr uint32_t kIdescS =                    // A = Q (TMEM), B = K (K-major)
+      kF16 ? ptx::idesc_f16(128, kN, 0, 0) : ptx::idesc_bf16(128, kN, 0, 0);
   constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
   constexpr uint32_t kOffMail = C::kOffMisc + kMiscMail;
   constexpr uint32_t kOffReq = C::kOffMisc + kMiscReq;
@@ -413,7 +487,9 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const int* pair_rank = reinterpret_cast<const int*>(p.ws + p.L.pair_rank);   // non-empty pairs before p
   const int lo = pair_lo[pl], hi = pair_lo[pl + 1];     // this pair's page range (cost-balanced by the planner)
   const int sq = p.sq;
-  const bool active = smem_ok && group < sq;
+  // the exact FP8 pass after an f16 pass runs only if that pass flagged an
+  // input outside the f16-exact range
+  const bool active = smem_ok && group < sq && !(p.fp8_fallback && hdr->fp8_range == 0);
 
   if (active && warp == 0) {
     // ------------------------------------------------------------ producer
@@ -521,7 +597,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
       }
     }
-  } else if (kMode == 1 && active && (warp >= 8 || (warp == 2 && rank == 1))) {
+  } else if (kMode >= 1 && active && (warp >= 8 || (warp == 2 && rank == 1))) {
     // ------------------------------------------------------------ FP8 dequant
     // raw half page -> rank 1: K slot (all 18 value groups, nine-chunk
     // layout); rank 0: V slot (the 16 latent groups).  Warp wq takes value
@@ -538,7 +614,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
     int vs = 0; uint32_t vphase = 0;      // rank 0: V slot
     int rs = 0; uint32_t rphase = 0;
-    bool ok = true;
+    bool ok = true, range_flagged = false;
     while (ok && w.next(sg)) {
       const int hp_end = 2 * sg.t1;
       for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
@@ -552,8 +628,12 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           uint32_t o0[16], o1[16];
           if (raw_flag[rs] == 0) {
             const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + t * kFp8Row;
-            dequant_group(row, g, o0);
-            dequant_group(row + 16 * kFp8Row, g, o1);
+            const bool r0 = dequant_group<kF16>(row, g, o0);
+            const bool r1 = dequant_group<kF16>(row + 16 * kFp8Row, g, o1);
+            if (kF16 && !range_flagged && __any_sync(0xffffffffu, !(r0 && r1))) {
+              if (lane == 0) atomicExch(&hdr->fp8_range, 1);
+              range_flagged = true;
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) { o0[e] = 0u; o1[e] = 0u; }
@@ -757,7 +837,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               for (int n = 0; n < 2; ++n) {
                 const uint64_t bdesc =
                     ptx::sdesc_sw128(vbase + static_cast<uint32_t>(s * 2) * kVGroup + n * 4 * kAtom, kAtom, kVGroup);
-                ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV, (h0 > 2 * sg.t0 || k > 0) ? 1u : 0u);
+                ptx::mma_ss(tmem + 256u * n, adesc, bdesc, kIdescPV<kMode>, (h0 > 2 * sg.t0 || k > 0) ? 1u : 0u);
               }
             }
             ptx::mma_commit(BAR(VEMPTY + vs));
@@ -806,9 +886,11 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const uint8_t* qa = reinterpret_cast<const uint8_t*>(p.q_abs + (static_cast<size_t>(row) * kHeads + h) * kDc);
         const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope + (static_cast<size_t>(row) * kHeads + h) * kDr);
         const uint32_t qaddr = tmem + lane_base + kQCol;
-        if (kSG == 1) load_q_chunks<0, 9>(qa, qr, qaddr);
-        else if (grp == 0) load_q_chunks<0, 5>(qa, qr, qaddr);
-        else load_q_chunks<5, 9>(qa, qr, qaddr);
+        float qmax = 0.f;
+        if (kSG == 1) load_q_chunks<0, 9, kF16>(qa, qr, qaddr, qmax);
+        else if (grp == 0) load_q_chunks<0, 5>(qa, qr, qaddr, qmax);
+        else load_q_chunks<5, 9>(qa, qr, qaddr, qmax);
+        if (kF16 && __any_sync(0xffffffffu, qmax > kF16Max) && lane == 0) atomicExch(&hdr->fp8_range, 1);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(BAR(QREADY));
@@ -857,7 +939,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         float alpha = 1.f;
         if (h0 == 2 * sg.t0) {
           m_ref = mx;
-        } else if ((mx - m_ref) * c > kRescaleThreshold) {
+        } else if ((mx - m_ref) * c > kRescaleThreshold<kMode>) {
           alpha = fast_exp2((m_ref - mx) * c);
           l *= alpha;
           m_ref = mx;
@@ -870,7 +952,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             float x0 = __uint_as_float(mine[2 * e]), x1 = __uint_as_float(mine[2 * e + 1]);
             sub_scale2(x0, x1, -m_ref, c);
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            pk[e] = pack_bf16x2(p0, p1);
+            pk[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             add2(la, lb, p0, p1);
           }
         } else {
@@ -879,7 +961,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             const int col = c_mine + 2 * e;
             const float p0 = col < valid ? fast_exp2((__uint_as_float(mine[2 * e]) - m_ref) * c) : 0.f;
             const float p1 = col + 1 < valid ? fast_exp2((__uint_as_float(mine[2 * e + 1]) - m_ref) * c) : 0.f;
-            pk[e] = pack_bf16x2(p0, p1);
+            pk[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             la += p0;
             lb += p1;
           }
@@ -1085,7 +1167,14 @@ cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tma
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return launch_decode_mode<1>(unused, unused, unused, p, n_pairs, pdl, stream);
+  // the f16-operand pass, then the exact bf16-operand pass, which returns at
+  // once unless the first pass flagged an input outside the f16-exact range
+  DecodeParams q = p;
+  q.fp8_fallback = 0;
+  cudaError_t e = launch_decode_mode<2>(unused, unused, unused, q, n_pairs, pdl, stream);
+  if (e != cudaSuccess) return e;
+  q.fp8_fallback = 1;
+  return launch_decode_mode<1>(unused, unused, unused, q, n_pairs, pdl, stream);
 }
 
 int decode_max_pairs() {

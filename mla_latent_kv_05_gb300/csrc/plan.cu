@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     hdr->n_comb = comb_total * sq;
     hdr->pairs_per_group = pairs_per_group;
     hdr->abort_flag = 0;
+    hdr->fp8_range = 0;
   }
 }
 

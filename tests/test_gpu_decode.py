@@ -266,6 +266,23 @@ def test_fp8_causal_and_unused_nan_codes(cuda_device):
     assert_close(out, lse, *ref)
 
 
+def test_fp8_query_beyond_f16_range_takes_the_exact_pass(cuda_device):
+    # The FP8 path computes with f16 operands when every scale exponent lies
+    # in [113, 134] and every query value fits f16; otherwise an exact pass
+    # with bf16 operands recomputes the call.  One query value of 1e5 (past
+    # the f16 maximum 65504) forces that pass.  Latent dimension 7 of every
+    # cached token is zero, so the scores keep their usual size and the
+    # result must still match the oracle (in f16 the product would be
+    # inf * 0 = NaN).
+    inp = gen.make_inputs(3, 1, [200, 64, 1], kv_dtype="fp8", seed=41)
+    inp.kv_cache[:, :, 7] = 0
+    inp.q_absorbed[1, 0, 5, 7] = 1.0e5
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, lse, *oracle(inp))
+
+
 def test_fp8_bad_page_sets_status(cuda_device):
     inp = gen.make_inputs(2, 1, [100, 64], kv_dtype="fp8", seed=4)
     inp.block_table[1, 0] = -3
