@@ -20,9 +20,11 @@ namespace mla {
 
 namespace {
 
-// Cost of starting a row segment, in pages: measured at 5-8 us per segment
-// against about 1.2 us per page on GB300.
-constexpr int kSegCost = 5;
+// Cost of starting a row segment, in pages.  Tuned on GB300 by timing the
+// attention kernel over 3..24: 8..12 are best on the ragged, uniform and
+// long causal workloads alike (a segment start costs a query load, a
+// pipeline refill and an output drain, about 10 us against 1.2 us per page).
+constexpr int kSegCost = 10;
 
 __device__ int block_exclusive_scan(int v, int* smem_warp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
   // Row costs for the partition: a row with pages costs its pages plus
   // kSegCost pages' worth for its segment start (query load, output write,
-  // pipeline refill), measured at about five pages on GB300.
+  // pipeline refill).
   int local_ne = 0;
   for (int b = lo; b < hi; ++b) local_ne += lens[b] > 0 ? 1 : 0;
   int ne_total = 0;
