@@ -187,3 +187,80 @@ def workload_counts(inp: DecodeInputs) -> dict:
     flops = pairs * 2 * H * (ROW_ELEMS + D_LATENT)
     return dict(kv_tokens=kv_tokens, query_token_pairs=pairs, bytes=bytes_,
                 flops=flops, kv_bytes=kv_tokens * row_bytes)
+
+
+# --------------------------------------------------------------------------
+# Sparse top-k decode inputs (DeepSeek-V3.2 record: index_topk 2048).  The
+# indexer's output is stood in for by seeded random picks: each query row
+# (b, i) gets up to topk distinct tokens drawn uniformly from the tokens
+# visible to it in its own context (the first seq_len - (Sq-1-i) tokens of
+# row b), given as physical cache slots (page * 64 + offset, read off the
+# block table) in a random order, padded with -1 when fewer than topk are
+# visible.
+# --------------------------------------------------------------------------
+
+@dataclass
+class SparseInputs:
+    dense: DecodeInputs          # cache, queries, context block table and lengths
+    token_slots: torch.Tensor    # int32 [B, Sq, topk]: cache slot or -1
+    topk: int
+    name: str = ""
+
+    @property
+    def batch(self) -> int:
+        return self.dense.batch
+
+    @property
+    def sq(self) -> int:
+        return self.dense.sq
+
+
+def make_sparse_inputs(batch: int, sq: int, context_lens, topk: int, kv_dtype: str = "bf16",
+                       seed: int = 0, pad_middle: bool = False, name: str = "") -> SparseInputs:
+    """Seeded sparse decode problem.  pad_middle: also scatter a few -1
+    entries inside the list (a stress case for the masking)."""
+    dense = make_inputs(batch, sq, context_lens, kv_dtype=kv_dtype, seed=seed)
+    gen = torch.Generator().manual_seed(int(seed) * 31 + 7)
+    slots = torch.full((batch, sq, topk), -1, dtype=torch.int32)
+    bt = dense.block_table.to(torch.int64)
+    for b in range(batch):
+        for i in range(sq):
+            vis = int(dense.seq_lens[b]) - (sq - 1 - i)
+            if vis <= 0:
+                continue
+            n = min(vis, topk)
+            pos = torch.randperm(vis, generator=gen)[:n]
+            s = bt[b, pos // PAGE_SIZE] * PAGE_SIZE + pos % PAGE_SIZE
+            slots[b, i, :n] = s.to(torch.int32)
+            if pad_middle and n > 4:
+                holes = torch.randperm(n, generator=gen)[: max(1, n // 16)]
+                slots[b, i, holes] = -1
+            slots[b, i] = slots[b, i, torch.randperm(topk, generator=gen)]
+    return SparseInputs(dense=dense, token_slots=slots, topk=int(topk), name=name)
+
+
+SPARSE_WORKLOADS = {
+    6: dict(name="sparse top-2048 B64 Sq1 over 32K contexts bf16", batch=64, sq=1, context=32768,
+            topk=2048, kv_dtype="bf16"),
+}
+
+
+def make_sparse_workload(workload: int) -> SparseInputs:
+    w = SPARSE_WORKLOADS[workload]
+    return make_sparse_inputs(w["batch"], w["sq"], [w["context"]] * w["batch"], w["topk"],
+                              kv_dtype=w["kv_dtype"], seed=seed_for(workload), name=w["name"])
+
+
+def sparse_counts(inp: SparseInputs) -> dict:
+    """Units of work of a sparse problem: listed tokens (query, token pairs),
+    algorithmic bytes (each listed cache row once, q, out, lse, the slot
+    lists) and FLOPs."""
+    d = inp.dense
+    H = int(d.q_absorbed.shape[2])
+    row_bytes = ROW_ELEMS * 2 if d.kv_dtype == "bf16" else FP8_ROW_BYTES
+    pairs = int((inp.token_slots >= 0).sum())
+    rows = inp.batch * inp.sq
+    bytes_ = (pairs * row_bytes + rows * H * (D_LATENT + D_ROPE) * 2 + rows * H * D_LATENT * 2 + rows * H * 4
+              + inp.token_slots.numel() * 4)
+    flops = pairs * 2 * H * (ROW_ELEMS + D_LATENT)
+    return dict(kv_tokens=pairs, query_token_pairs=pairs, bytes=bytes_, flops=flops, kv_bytes=pairs * row_bytes)

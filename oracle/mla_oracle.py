@@ -156,3 +156,48 @@ def attend_unabsorbed(q_nope: np.ndarray, q_rope: np.ndarray, c_kv: np.ndarray,
 def up_project_output(out_latent: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
     """Apply W_i^UV to the latent output of each head: [H, 512] -> [H, d_h]."""
     return np.einsum("hkc,hc->hk", w_uv, out_latent)
+
+
+# --------------------------------------------------------------------------
+# Sparse top-k decode ("DeepSeek-V3.2" record: the sparse attention indexer,
+# config index_topk 2048 -- a lightweight selector picks a candidate set of
+# cached tokens and attention runs over that set instead of the whole
+# context; the latent rows are cached per token as before).
+#
+# Readings where the record is silent (listed again in the design notes):
+#   * the selector's output reaches the attention as, per query row, a list
+#     of topk physical cache slots, slot = page * page_size + offset into the
+#     paged cache; -1 means "no token" (fewer candidates than topk);
+#   * attention runs over the listed tokens as given: no further causal
+#     mask, and a slot listed twice counts twice;
+#   * scale, LSE and the empty-row convention are those of the dense decode.
+# --------------------------------------------------------------------------
+
+def sparse_gather_rows(rows: np.ndarray, slots: np.ndarray) -> np.ndarray:
+    """The rows of the listed cache slots, in list order, skipping -1.
+    rows [P, page, 576]; slots [topk] int -> [n, 576]."""
+    flat = rows.reshape(-1, rows.shape[-1])
+    s = np.asarray(slots, dtype=np.int64)
+    s = s[s >= 0]
+    assert np.all(s < flat.shape[0]), "slot past the cache"
+    return flat[s]
+
+
+def mla_decode_sparse(q_abs: np.ndarray, q_rope: np.ndarray, rows: np.ndarray,
+                      token_slots: np.ndarray, scale: float, query_rows=None):
+    """Sparse decode: query row (b, i) attends over the cache slots
+    token_slots[b, i, :] (see the readings above).
+
+    q_abs [B, Sq, H, 512], q_rope [B, Sq, H, 64], rows [P, page, 576] as in
+    cache_rows, token_slots [B, Sq, topk].  Returns out [B, Sq, H, 512],
+    lse [B, Sq, H] (rows not in query_rows are left NaN).
+    """
+    B, Sq, H, _ = q_abs.shape
+    out = np.full((B, Sq, H, D_LATENT), np.nan)
+    lse = np.full((B, Sq, H), np.nan)
+    todo = query_rows if query_rows is not None else [
+        (b, i) for b in range(B) for i in range(Sq)]
+    for b, i in todo:
+        g = sparse_gather_rows(rows, token_slots[b, i])
+        out[b, i], lse[b, i] = attend_latent(q_abs[b, i], q_rope[b, i], g, scale)
+    return out, lse

@@ -304,3 +304,108 @@ def _marker_gather_ok(gather):
 
 def test_gather_by_markers():
     assert _marker_gather_ok(mla_oracle.gather_rows)
+
+
+# ----------------------------------------------------------------- sparse top-k
+def _context_slots(bt_row, n, page=64):
+    """Cache slots of the first n tokens of a row (block-table order)."""
+    j = np.arange(n)
+    return np.asarray(bt_row, dtype=np.int64)[j // page] * page + j % page
+
+
+def test_sparse_listing_the_visible_context_equals_dense_decode():
+    # Listing exactly the tokens a dense query sees (any order, -1 padded)
+    # must reproduce the dense decode, which is pinned to torch's SDPA above.
+    inp = gen.make_inputs(3, 2, [70, 1, 200], seed=21)
+    rows = mla_oracle.cache_rows(_f64(inp.kv_cache), "bf16")
+    qa, qr = _f64(inp.q_absorbed), _f64(inp.q_rope)
+    bt, sl = inp.block_table.numpy(), inp.seq_lens.numpy()
+    out, lse = mla_oracle.mla_decode(qa, qr, rows, bt, sl, inp.scale)
+    topk = 256
+    slots = np.full((3, 2, topk), -1, dtype=np.int64)
+    rng = np.random.default_rng(5)
+    for b in range(3):
+        for i in range(2):
+            n = max(int(sl[b]) - (2 - 1 - i), 0)
+            s = _context_slots(bt[b], n)
+            slots[b, i, :n] = s
+            slots[b, i] = rng.permutation(slots[b, i])
+    out2, lse2 = mla_oracle.mla_decode_sparse(qa, qr, rows, slots, inp.scale)
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(out2, out, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(lse2[fin], lse[fin], rtol=1e-13)
+    assert np.all(np.isneginf(lse2[~fin])) and np.all(out2[~fin] == 0)
+
+
+def test_sparse_order_padding_and_split_invariance():
+    inp = gen.make_sparse_inputs(2, 1, [500, 130], 96, seed=22, pad_middle=True)
+    d = inp.dense
+    rows = mla_oracle.cache_rows(_f64(d.kv_cache), "bf16")
+    qa, qr = _f64(d.q_absorbed), _f64(d.q_rope)
+    slots = inp.token_slots.numpy()
+    out, lse = mla_oracle.mla_decode_sparse(qa, qr, rows, slots, d.scale)
+    rng = np.random.default_rng(6)
+    perm = np.stack([[rng.permutation(slots[b, 0])] for b in range(2)])
+    out2, lse2 = mla_oracle.mla_decode_sparse(qa, qr, rows, perm, d.scale)
+    np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-14)
+    # two halves of the list merged by the LSE rule equal the whole list
+    for b in range(2):
+        h = slots.shape[-1] // 2
+        parts = [mla_oracle.mla_decode_sparse(qa[b:b + 1], qr[b:b + 1], rows, slots[b:b + 1, :, a:e], d.scale)
+                 for a, e in ((0, h), (h, slots.shape[-1]))]
+        o, l = mla_oracle.merge_partials(np.stack([p[0][0, 0] for p in parts]), np.stack([p[1][0, 0] for p in parts]))
+        np.testing.assert_allclose(o, out[b, 0], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(l, lse[b, 0], rtol=1e-13)
+
+
+def test_sparse_duplicates_count_twice_and_minus_one_is_skipped():
+    # Two tokens A, B; the list [A, -1, A, B] gives weights 2 e^sA : e^sB.
+    rng = np.random.default_rng(7)
+    rows = rng.standard_normal((1, 64, 576))
+    qa, qr = rng.standard_normal((1, 1, 2, 512)), rng.standard_normal((1, 1, 2, 64))
+    A, B, scale = 5, 17, 0.05
+    out, lse = mla_oracle.mla_decode_sparse(qa, qr, rows, np.array([[[A, -1, A, B]]]), scale)
+    for h in range(2):
+        sa = scale * (qa[0, 0, h] @ rows[0, A, :512] + qr[0, 0, h] @ rows[0, A, 512:])
+        sb = scale * (qa[0, 0, h] @ rows[0, B, :512] + qr[0, 0, h] @ rows[0, B, 512:])
+        z = 2 * math.exp(sa) + math.exp(sb)
+        want = (2 * math.exp(sa) * rows[0, A, :512] + math.exp(sb) * rows[0, B, :512]) / z
+        np.testing.assert_allclose(out[0, 0, h], want, rtol=1e-12, atol=1e-14)
+        assert abs(lse[0, 0, h] - math.log(z)) < 1e-12
+    out, lse = mla_oracle.mla_decode_sparse(qa, qr, rows, np.full((1, 1, 8), -1), scale)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def _sparse_marker_gather_ok(gather):
+    """Fill every cache slot with its own slot number; gathering a list must
+    return exactly the listed slots, in order, without the -1 entries."""
+    rows = np.arange(5 * 64, dtype=np.float64).reshape(5, 64, 1) * np.ones((1, 1, 576))
+    rng = np.random.default_rng(8)
+    for _ in range(20):
+        lst = rng.integers(0, 5 * 64, size=37)
+        lst[rng.integers(0, 37, size=5)] = -1
+        g = gather(rows, lst)
+        want = lst[lst >= 0]
+        if g.shape[0] != want.size or not np.array_equal(g[:, 0], want) or not np.all(g == g[:, :1]):
+            return False
+    return True
+
+
+def test_sparse_gather_by_markers_catches_planted_mistakes():
+    assert _sparse_marker_gather_ok(mla_oracle.sparse_gather_rows)
+
+    def keeps_minus_one(rows, slots):        # -1 read as the last slot
+        return rows.reshape(-1, rows.shape[-1])[np.asarray(slots, dtype=np.int64)]
+
+    def sorted_slots(rows, slots):           # order lost (harmless for attention, caught here)
+        s = np.sort(np.asarray(slots, dtype=np.int64))
+        return rows.reshape(-1, rows.shape[-1])[s[s >= 0]]
+
+    def page_major_swap(rows, slots):        # slot read as offset * pages + page
+        s = np.asarray(slots, dtype=np.int64)
+        s = s[s >= 0]
+        return rows[s % rows.shape[0], s // rows.shape[0]]
+
+    for bad in (keeps_minus_one, sorted_slots, page_major_swap):
+        assert not _sparse_marker_gather_ok(bad), bad.__name__
