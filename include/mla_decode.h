@@ -66,7 +66,8 @@ typedef enum {
   MLA_ERR_CUDA = -4,          /* a CUDA runtime call failed                   */
   MLA_STATUS_BAD_PAGE = -5,   /* device: block-table entry out of range       */
   MLA_STATUS_TIMEOUT = -6,    /* device: a pipeline wait gave up              */
-  MLA_STATUS_BAD_SEQ_LEN = -7 /* device: seq_len outside [0, max_pages*64]    */
+  MLA_STATUS_BAD_SEQ_LEN = -7, /* device: seq_len outside [0, max_pages*64]   */
+  MLA_STATUS_BAD_INDEX = -8    /* device: sparse token slot outside [-1, num_pages*64) */
 } mla_status;
 
 /* Bytes of device workspace a decode call with these sizes needs on the
@@ -124,14 +125,38 @@ int mla_decode_bf16_noalloc(const uint16_t* q_absorbed, const uint16_t* q_rope,
 /* Same over the FP8 cache: each 594-byte row is dequantised as
  * v[k] = e4m3(byte[k]) * 2^(byte[576 + k/32] - 127) ("DeepSeek-R1" model
  * record, engine kernel constraint (2): e4m3 values, one e8m0 scale per 32)
- * and then attended exactly as the bf16 path (the dequantised values are
- * exact in bf16).  kv_cache must be 16-byte aligned. */
+ * and then attended as the bf16 path does.  The dequantised values are exact
+ * in bf16; when every scale exponent of the call lies in [113, 134] and every
+ * query value fits f16 they are exact in f16 too, and the MMAs take f16
+ * operands (the query and the softmax weights rounded to f16 instead of
+ * bf16); otherwise a second pass recomputes the call with bf16 operands.
+ * kv_cache must be 16-byte aligned. */
 int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope,
                    const uint8_t* kv_cache, const int32_t* block_table,
                    const int32_t* seq_lens, int batch, int sq, int num_heads,
                    int num_pages, int page_size, int max_pages,
                    float softmax_scale, uint16_t* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Sparse top-k decode ("DeepSeek-V3.2" model record: the sparse attention
+ * indexer, index_topk 2048, selects the candidate tokens each query attends
+ * over; the latent rows stay cached per token).  Query row (b, i) attends
+ * over the tokens listed in token_slots[b][i][0..topk): each entry is a
+ * physical cache slot, page * 64 + offset into kv_cache (bf16
+ * [num_pages, 64, 576]), or -1 for "no token".  No other mask applies; a
+ * slot listed twice counts twice.  The scores, softmax, out and lse are
+ * those of mla_decode_bf16.  A row with no listed token gets out = 0 and
+ * lse = -inf.  An entry outside [-1, num_pages*64) is skipped and sets
+ * MLA_STATUS_BAD_INDEX.
+ * token_slots: int32 [batch, sq, topk], device; 1 <= topk <= 16384.
+ * workspace: mla_workspace_size_sparse(...) bytes, 256-byte aligned. */
+int mla_workspace_size_sparse(int batch, int sq, int topk, int num_heads, int page_size, size_t* bytes);
+int mla_decode_sparse_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                           const uint16_t* kv_cache, const int32_t* token_slots,
+                           int batch, int sq, int topk, int num_heads,
+                           int num_pages, int page_size, float softmax_scale,
+                           uint16_t* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* Merge split-KV partial results (attention over disjoint token sets):
  *   L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * partial_out_s,

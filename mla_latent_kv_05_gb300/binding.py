@@ -18,6 +18,7 @@ MLA_OK = 0
 _STATUS = {
     0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED", -3: "MLA_ERR_WORKSPACE",
     -4: "MLA_ERR_CUDA", -5: "MLA_STATUS_BAD_PAGE", -6: "MLA_STATUS_TIMEOUT", -7: "MLA_STATUS_BAD_SEQ_LEN",
+    -8: "MLA_STATUS_BAD_INDEX",
 }
 
 # Exported entry points and their C signatures (restype, argtypes).
@@ -31,6 +32,9 @@ SIGNATURES = {
                                      _P]),
     "mla_decode_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                             ctypes.c_size_t, _P]),
+    "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    "mla_decode_sparse_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                                    ctypes.c_size_t, _P]),
     "mla_combine_splits": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
     "mla_get_status": (_I, [_P, _P]),
     "mla_profile_next_decode": (_I, [_P, _P]),
@@ -190,6 +194,55 @@ def mla_decode_fp8(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, o
     576 e4m3 codes then 18 e8m0 scales); returns (out, lse)."""
     return _decode("mla_decode_fp8", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
                    workspace, stream, torch.uint8, 594)
+
+
+def mla_workspace_size_sparse(batch: int, sq: int, topk: int, num_heads: int = 128, page_size: int = 64) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load().mla_workspace_size_sparse(int(batch), int(sq), int(topk), int(num_heads), int(page_size),
+                                          ctypes.byref(n))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_workspace_size_sparse")
+    return int(n.value)
+
+
+def alloc_workspace_sparse(batch: int, sq: int, topk: int, device=None) -> torch.Tensor:
+    """A zeroed workspace buffer (uint8) for the sparse decode."""
+    n = mla_workspace_size_sparse(batch, sq, topk)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_decode_sparse_bf16(q_absorbed, q_rope, kv_cache, token_slots, scale, out=None, lse=None,
+                           workspace=None, stream=None):
+    """Sparse top-k decode over a bf16 latent cache [num_pages, 64, 576]:
+    query row (b, i) attends over the cache slots token_slots[b, i, :]
+    (int32 [B, Sq, topk], slot = page * 64 + offset, -1 = no token).
+    Returns (out, lse)."""
+    B, Sq, H, D = q_absorbed.shape
+    _check(q_absorbed, "q_absorbed", torch.bfloat16, (B, Sq, H, 512))
+    _check(q_rope, "q_rope", torch.bfloat16, (B, Sq, H, 64))
+    _check(kv_cache, "kv_cache", torch.bfloat16)
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != 576:
+        raise ValueError(f"kv_cache must be [num_pages, page_size, 576], got {tuple(kv_cache.shape)}")
+    _check(token_slots, "token_slots", torch.int32)
+    if token_slots.dim() != 3 or tuple(token_slots.shape[:2]) != (B, Sq):
+        raise ValueError("token_slots must be [B, Sq, topk]")
+    topk = int(token_slots.shape[2])
+    if out is None:
+        out = torch.empty((B, Sq, H, 512), dtype=torch.bfloat16, device=q_absorbed.device)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=q_absorbed.device)
+    _check(out, "out", torch.bfloat16, (B, Sq, H, 512))
+    _check(lse, "lse", torch.float32, (B, Sq, H))
+    if workspace is None:
+        workspace = alloc_workspace_sparse(B, Sq, topk, q_absorbed.device)
+    _check(workspace, "workspace", torch.uint8)
+    rc = load().mla_decode_sparse_bf16(
+        _ptr(q_absorbed), _ptr(q_rope), _ptr(kv_cache), _ptr(token_slots), int(B), int(Sq), topk, int(H),
+        int(kv_cache.shape[0]), int(kv_cache.shape[1]), ctypes.c_float(float(scale)), _ptr(out), _ptr(lse),
+        _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_sparse_bf16")
+    return out, lse
 
 
 def mla_combine_splits(partial_out, partial_lse, split_indptr, out=None, lse=None, stream=None):

@@ -99,6 +99,9 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
   p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
   p.kv_fp8 = fp8 ? static_cast<const uint8_t*>(kv_cache) : nullptr;
+  p.kv_bf16 = fp8 ? nullptr : static_cast<const uint8_t*>(kv_cache);
+  p.sp_slots = nullptr;
+  p.topk = 0;
   p.block_table = block_table;
   p.batch = batch;
   p.sq = sq;
@@ -160,9 +163,82 @@ int static_scratch(void** ptr) {
   return MLA_OK;
 }
 
+constexpr int kMaxTopk = 16384;
+
+// Sparse top-k decode: compact the slot lists, plan the B*Sq query rows as a
+// batch of rows with one query each, gather-attend, merge.
+int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache, const int32_t* token_slots,
+               int batch, int sq, int topk, int num_heads, int num_pages, int page_size, float softmax_scale,
+               uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  if (!q_absorbed || !q_rope || !kv_cache || !token_slots || !out || !lse || !workspace) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || sq <= 0 || topk <= 0 || num_pages <= 0 || !std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (num_heads != kHeads || page_size != kPage || topk > kMaxTopk) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(batch) * sq > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_pages) * kPage >= INT_MAX / 2) return MLA_ERR_UNSUPPORTED;
+  if (!aligned(q_absorbed, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(token_slots, 4) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int pairs = decode_max_pairs();
+  if (pairs <= 0) return MLA_ERR_CUDA;
+  const int rows = batch * sq;
+  const WsLayout L = ws_layout(rows, 1, pairs, topk);
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  const int max_pages = (topk + kPage - 1) / kPage;
+  if (launch_sparse_prep(token_slots, rows, topk, num_pages * kPage, workspace, L, stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  const int32_t* counts = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(workspace) + L.sp_lens);
+  if (launch_plan(counts, rows, 1, max_pages, pairs, workspace, L, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
+  p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
+  p.kv_bf16 = static_cast<const uint8_t*>(kv_cache);
+  p.block_table = nullptr;
+  p.batch = rows;
+  p.sq = 1;
+  p.num_pages = num_pages;
+  p.max_pages = max_pages;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.sp_slots = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(workspace) + L.sp_slots);
+  p.topk = topk;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.ws = static_cast<uint8_t*>(workspace);
+  p.L = L;
+  cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
+  g_prof_before = g_prof_after = nullptr;
+  const bool pdl = ev0 == nullptr;
+  if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode_sparse(p, pairs, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine_plan(workspace, L, rows, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int mla_workspace_size_sparse(int batch, int sq, int topk, int num_heads, int page_size, size_t* bytes) {
+  if (!bytes || batch < 0 || sq <= 0 || topk <= 0) return MLA_ERR_INVALID_ARG;
+  if (num_heads != kHeads || page_size != kPage || topk > kMaxTopk) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(batch) * sq > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  const int pairs = decode_max_pairs();
+  if (pairs <= 0) return MLA_ERR_CUDA;
+  *bytes = ws_layout(batch > 0 ? batch * sq : 1, 1, pairs, topk).total;
+  return MLA_OK;
+}
+
+int mla_decode_sparse_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint16_t* kv_cache,
+                           const int32_t* token_slots, int batch, int sq, int topk, int num_heads, int num_pages,
+                           int page_size, float softmax_scale, uint16_t* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return run_sparse(q_absorbed, q_rope, kv_cache, token_slots, batch, sq, topk, num_heads, num_pages, page_size,
+                    softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
 
 int mla_workspace_size(int batch, int sq, int num_heads, int page_size, size_t* bytes) {
   if (!bytes || batch < 0 || sq <= 0) return MLA_ERR_INVALID_ARG;
@@ -257,6 +333,7 @@ const char* mla_status_string(int code) {
     case MLA_STATUS_BAD_PAGE: return "MLA_STATUS_BAD_PAGE";
     case MLA_STATUS_TIMEOUT: return "MLA_STATUS_TIMEOUT";
     case MLA_STATUS_BAD_SEQ_LEN: return "MLA_STATUS_BAD_SEQ_LEN";
+    case MLA_STATUS_BAD_INDEX: return "MLA_STATUS_BAD_INDEX";
     default: return "MLA_UNKNOWN_STATUS";
   }
 }

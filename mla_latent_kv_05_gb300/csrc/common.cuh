@@ -35,13 +35,17 @@ struct PlanHeader {
 // Offsets (bytes) of the plan arrays and split partials inside the workspace.
 struct WsLayout {
   size_t lens, tile_start, row_cost, pair_lo, pair_rank, first_pair, slot_base, comb_row, comb_start, comb_count;
-  size_t part_lse, part_out, total;
+  size_t part_lse, part_out;
+  size_t sp_lens, sp_slots;   // sparse decode: listed tokens per row, compacted slot lists [rows, topk]
+  size_t total;
   int max_slots;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-__host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs) {
+// topk > 0: the sparse decode's extra arrays (its rows are batch * sq query
+// rows, planned as a batch of that many rows with one query each)
+__host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs, int topk = 0) {
   WsLayout L;
   const int pg = pairs / sq > 0 ? pairs / sq : 1;
   // every pair boundary splits at most one row: slots per query <= 2*(pg-1)
@@ -59,6 +63,8 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs) {
   L.comb_count = o;  o = align256(o + sizeof(int) * batch * sq);
   L.part_lse = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads);
   L.part_out = o;    o = align256(o + 2 * static_cast<size_t>(L.max_slots) * kHeads * kDc);   // bf16 partials
+  L.sp_lens = o;     o = align256(o + (topk > 0 ? sizeof(int) * batch : 0));
+  L.sp_slots = o;    o = align256(o + (topk > 0 ? sizeof(int) * static_cast<size_t>(batch) * topk : 0));
   L.total = o;
   return L;
 }

@@ -129,6 +129,9 @@ template <> struct Cfg<1> {
   static constexpr int kEpWarps = 4;           // rank 0: four epilogue warps (512 columns each)
 };
 template <> struct Cfg<2> : Cfg<1> {};
+// sparse decode over the bf16 cache: the bf16 plan, K and V gathered by rows
+template <> struct Cfg<3> : Cfg<0> {};
+constexpr int kGatherWarps = 3;          // sparse: warps 0, 2, 3 of each rank copy one half page of a tile each
 constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
 constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
 constexpr uint32_t kMiscMail = 1024;     // rank 0: fp32 1/l [2][128]
@@ -366,8 +369,7 @@ __device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* 
       for (int i = 0; i < 32; ++i) r0[i] = bf16x2_to_f16x2(r0[i], qmax);
       ptx::tmem_st32(taddr + 32u * c, r0);
     }
-    return;
-  }
+  } else {
 #pragma unroll 1
   for (int c = C0; c < C1; c += 2) {
     uint32_t r0[32], r1[32];
@@ -381,13 +383,15 @@ __device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* 
     ptx::tmem_st32(taddr + 32u * c, r0);
     if (two) ptx::tmem_st32(taddr + 32u * (c + 1), r1);
   }
+  }
 }
 
 }  // namespace dk
 
 // kMode 0: bf16 cache via TMA; 1: FP8 cache via bulk copies + dequant to
 // bf16 operands; 2: FP8 cache with f16 operands (flags inputs outside the
-// f16-exact range, which mode 1 then recomputes)
+// f16-exact range, which mode 1 then recomputes); 3: sparse top-k decode
+// over the bf16 cache (rows gathered by listed slot with 16-byte cp.async)
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dk::Cfg<kMode>::kThreads, 1)
 mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_kb,
@@ -399,6 +403,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   constexpr int kSG = C::kSmGroups;             // softmax warp groups
   constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
+  constexpr bool kFp8 = kMode == 1 || kMode == 2;  // FP8 cache (raw rings, dequant warps)
   constexpr bool kF16 = kMode == 2;               // FP8 with f16 operands
   constexpr uint32_t kIdescS =                    // A = Q (TMEM), B = K (K-major)
       kF16 ? ptx::idesc_f16(128, kN, 0, 0) : ptx::idesc_bf16(128, kN, 0, 0);
@@ -434,15 +439,17 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     const uint32_t dq = static_cast<uint32_t>(rank == 1 ? C::kDqWarps1 : C::kDqWarps0);
     constexpr uint32_t kEp = static_cast<uint32_t>(C::kEpWarps);
     // K tiles: the TMA bytes (bf16) or the dequant warps (FP8)
+    // sparse: each gather thread arrives once per tile (cp.async noinc)
+    constexpr uint32_t kGatherThreads = 32u * kGatherWarps;
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(BAR(KFULL + s), kMode == 0 ? 1u : dq);
+      ptx::mbar_init(BAR(KFULL + s), kFp8 ? dq : (kMode == 3 ? kGatherThreads : 1u));
       ptx::mbar_init(BAR(KEMPTY + s), 1);
-      ptx::mbar_init(BAR(KFULLB + s), 1);
+      ptx::mbar_init(BAR(KFULLB + s), kMode == 3 ? kGatherThreads : 1u);
       ptx::mbar_init(BAR(KEMPTYB + s), 1);
     }
     // V slots: the TMA bytes (bf16) or the dequant warps (FP8)
     for (int s = 0; s < kMaxVSlots; ++s) {
-      ptx::mbar_init(BAR(VFULL + s), kMode == 0 ? 1u : dq);
+      ptx::mbar_init(BAR(VFULL + s), kFp8 ? dq : (kMode == 3 ? 32u : 1u));   // sparse: one warp per half page
       ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
@@ -456,7 +463,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     for (int s = 0; s < kMailSlots; ++s) { ptx::mbar_init(BAR(MBFULL + s), 128); ptx::mbar_init(BAR(MBEMPTY + s), kEp); }
     for (int s = 0; s < kMaxRaw; ++s) {
       ptx::mbar_init(BAR(RAWFULL + s), 1);
-      ptx::mbar_init(BAR(RAWEMPTY + s), kMode == 0 ? 1u : dq);
+      ptx::mbar_init(BAR(RAWEMPTY + s), kFp8 ? dq : 1u);
     }
     ptx::fence_barrier_init();
   }
@@ -491,7 +498,80 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   // input outside the f16-exact range
   const bool active = smem_ok && group < sq && !(p.fp8_fallback && hdr->fp8_range == 0);
 
-  if (active && warp == 0) {
+  if (kMode == 3 && active && (warp == 0 || warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ sparse gather (both ranks)
+    // Warp gw copies half page gw of every tile: the row-local tokens
+    // [32 (h0 + gw), +32) of the segment's row, whose cache slots come from
+    // the compacted list.  One cache row is 1152 contiguous bytes; the lanes
+    // copy consecutive 16-byte pieces of it (coalesced), each into its
+    // 128B-swizzled place: rank 1 the A part (chunks 0..4) and B part
+    // (chunks 5..8) blocks of the K tile buffer, rank 0 the eight latent
+    // chunks of a V slot.  Completion is counted per thread with
+    // cp.async.mbarrier.arrive.noinc; the MMA issuers fence the generic and
+    // async proxies after their waits.  Tokens past the row's count are not
+    // copied (the softmax masks them; the value SM zeroes their V rows).
+    const int gw = warp == 0 ? 0 : warp - 1;
+    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    Segment sg;
+    int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
+    int vs = 0; uint32_t vphase = 0;      // rank 0: V ring head
+    bool ok = true;
+    while (ok && w.next(sg)) {
+      const int len = lens[sg.b];
+      const int32_t* slots = p.sp_slots + static_cast<size_t>(sg.b) * p.topk;
+      const int hp_end = 2 * sg.t1;
+      for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
+        const int nh = min(TH, hp_end - h0);
+        const int r0 = (h0 + gw) * kHalf;                       // row-local index of this warp's first token
+        const int n_rows = gw < nh ? max(0, min(kHalf, len - r0)) : 0;
+        const int my_slot = lane < n_rows ? __ldg(slots + r0 + lane) : 0;
+        const int c = lane >> 3, q = lane & 7;                  // chunk (of four) and 16-byte piece of a lane
+        if (rank == 1) {
+          const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);
+          if (!wait_warp<false>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+          for (int i = 0; i < n_rows; ++i) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+            const uint8_t* src = p.kv_bf16 + static_cast<size_t>(slot) * (kRow * 2);
+            const int r = gw * kHalf + i;                        // row of the tile
+            const uint32_t row = tbase + static_cast<uint32_t>(r >> 3) * (5 * kAtom) + (r & 7) * 128;
+            ptx::cp_async_16(row + c * kAtom + ((q ^ (r & 7)) << 4), src + c * 128 + q * 16);
+            if (lane < 8) ptx::cp_async_16(row + 4 * kAtom + ((q ^ (r & 7)) << 4), src + 4 * 128 + q * 16);
+          }
+          ptx::cp_async_arrive_noinc(BAR(KFULL + kb));
+          if (!wait_warp<false>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+          for (int i = 0; i < n_rows; ++i) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+            const uint8_t* src = p.kv_bf16 + static_cast<size_t>(slot) * (kRow * 2);
+            const int r = gw * kHalf + i;
+            const uint32_t row = tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(r >> 3) * (4 * kAtom) +
+                                 (r & 7) * 128;
+            ptx::cp_async_16(row + c * kAtom + ((q ^ (r & 7)) << 4), src + (5 + c) * 128 + q * 16);
+          }
+          ptx::cp_async_arrive_noinc(BAR(KFULLB + kb));
+          kb ^= 1;
+          if (kb == 0) kphase ^= 1u;
+        } else {
+          if (gw < nh) {
+            int v = vs + gw;
+            uint32_t vp = vphase;
+            if (v >= kVSlots) { v -= kVSlots; vp ^= 1u; }
+            if (!wait_warp<false>(BAR(VEMPTY + v), vp ^ 1u, hdr)) { ok = false; break; }
+            const uint32_t vbase = sbase + static_cast<uint32_t>(v) * kVSlot;
+            for (int i = 0; i < n_rows; ++i) {
+              const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+              const uint8_t* src = p.kv_bf16 + static_cast<size_t>(slot) * (kRow * 2);
+              const uint32_t row = vbase + static_cast<uint32_t>(i >> 3) * kVGroup + (i & 7) * 128;
+              ptx::cp_async_16(row + c * kAtom + ((q ^ (i & 7)) << 4), src + c * 128 + q * 16);
+              ptx::cp_async_16(row + (c + 4) * kAtom + ((q ^ (i & 7)) << 4), src + (c + 4) * 128 + q * 16);
+            }
+            ptx::cp_async_arrive_noinc(BAR(VFULL + v));
+          }
+          vs += nh;
+          if (vs >= kVSlots) { vs -= kVSlots; vphase ^= 1u; }
+        }
+      }
+    }
+  } else if (kMode != 3 && active && warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_normal();
@@ -597,7 +677,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
       }
     }
-  } else if (kMode >= 1 && active && (warp >= 8 || (warp == 2 && rank == 1))) {
+  } else if (kFp8 && active && (warp >= 8 || (warp == 2 && rank == 1))) {
     // ------------------------------------------------------------ FP8 dequant
     // raw half page -> rank 1: K slot (all 18 value groups, nine-chunk
     // layout); rank 0: V slot (the 16 latent groups).  Warp wq takes value
@@ -727,7 +807,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             !wait_warp<false>(BAR(SEMPTY + sb), sphase ^ 1u, hdr)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t d = tmem + kSCol + static_cast<uint32_t>(kN * sb);
-        if constexpr (kMode == 0) {
+        if constexpr (kMode == 0 || kMode == 3) {
+          if constexpr (kMode == 3) ptx::fence_proxy_async_cta();   // rows written by cp.async
           // A part (K-steps 0..19, chunks 0..4, 5 KiB per row group), then
           // B part (K-steps 20..35, chunks 5..8, 4 KiB per row group); the
           // A part's slots are released as soon as its MMAs are done
@@ -743,13 +824,16 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           __syncwarp();
           if (!wait_warp<false>(BAR(KFULLB + kb), kphase, hdr)) { ok = false; break; }
           ptx::tc_fence_after();
+          if constexpr (kMode == 3) ptx::fence_proxy_async_cta();
           if (lane == 0) {
             const uint64_t db = ptx::sdesc_sw128(tbase + static_cast<uint32_t>(TH) * kKA, 16, 4 * kAtom);
 #pragma unroll
             for (int k = 20; k < kRow / 16; ++k)
               ptx::mma_ts(d, tmem + kQCol + 8u * k,
                           db + static_cast<uint64_t>((((k >> 2) - 5) * kAtom + (k & 3) * 32) >> 4), kIdescS, 1u);
-            ptx::mma_commit_mc(BAR(KEMPTYB + kb), static_cast<uint16_t>(1u));   // rank 0 issues the B loads
+            // bf16: rank 0 issues the B loads; sparse: this CTA gathers them
+            if constexpr (kMode == 3) ptx::mma_commit(BAR(KEMPTYB + kb));
+            else ptx::mma_commit_mc(BAR(KEMPTYB + kb), static_cast<uint16_t>(1u));
             ptx::mma_commit(BAR(SFULL + sb));
           }
         } else if (lane == 0) {
@@ -813,6 +897,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const uint32_t pbase = sbase + C::kOffP + static_cast<uint32_t>(ps) * C::kPSlotBytes;
         for (int j = 0; j < nh; ++j) {
           if (!wait_warp<false>(BAR(VFULL + vs), vphase, hdr)) { ok = false; break; }
+          if constexpr (kMode == 3) ptx::fence_proxy_async_cta();   // rows written by cp.async
           const int valid = len_i - (h0 + j) * kHalf;   // tokens of this half page visible to the query
           if (valid < kHalf) {
             // rows past the visible length get P = 0; make their V finite too
@@ -1175,6 +1260,12 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cuda
   if (e != cudaSuccess) return e;
   q.fp8_fallback = 1;
   return launch_decode_mode<1>(unused, unused, unused, q, n_pairs, pdl, stream);
+}
+
+cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  return launch_decode_mode<3>(unused, unused, unused, p, n_pairs, pdl, stream);
 }
 
 int decode_max_pairs() {

@@ -11,10 +11,13 @@ struct DecodeParams {
   const __nv_bfloat16* q_abs;    // [B, Sq, 128, 512]
   const __nv_bfloat16* q_rope;   // [B, Sq, 128, 64]
   const uint8_t* kv_fp8;         // fp8 cache [P, 64, 594] (fp8 mode)
+  const uint8_t* kv_bf16;        // bf16 cache [P, 64, 576] (read by address in the sparse mode)
   const int32_t* block_table;    // [B, max_pages]
   int batch, sq, num_pages, max_pages;
   float scale_log2;              // softmax scale * log2(e)
   int fp8_fallback;              // FP8 exact pass: run only if the f16 pass flagged its inputs
+  const int32_t* sp_slots;       // sparse decode: compacted slot lists [rows, topk] (workspace)
+  int topk;
   __nv_bfloat16* out;            // [B, Sq, 128, 512]
   float* lse;                    // [B, Sq, 128]
   uint8_t* ws;
@@ -23,6 +26,9 @@ struct DecodeParams {
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_pages, int pairs_per_group,
                         void* ws, const WsLayout& L, cudaStream_t stream);
+// Sparse decode: compact each query row's listed slots into the workspace.
+cudaError_t launch_sparse_prep(const int32_t* token_slots, int rows, int topk, int num_slots, void* ws,
+                               const WsLayout& L, cudaStream_t stream);
 // pdl: launch as a programmatic dependent of the planner (the kernel waits on
 // griddepcontrol before reading the plan)
 // tmap_k / tmap_kb: half-page boxes of chunks 0..4 / 5..8 (score SM);
@@ -30,6 +36,9 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_page
 cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
                                const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
+// Sparse decode over the bf16 cache (p.kv_bf16, p.sp_slots; rows planned
+// with one query each).
+cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 int decode_max_pairs();
 cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows, __nv_bfloat16* out, float* lse,
                                 bool pdl, cudaStream_t stream);

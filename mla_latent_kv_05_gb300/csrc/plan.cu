@@ -206,7 +206,39 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
 }
 
+// Sparse decode: one CTA per query row compacts the row's listed cache slots
+// (list order kept, -1 entries dropped) into the workspace and counts them;
+// the planner then treats the count as the row's length.  An entry outside
+// [-1, num_slots) is dropped too and recorded as MLA_STATUS_BAD_INDEX.
+__global__ void __launch_bounds__(256) sparse_prep_kernel(const int32_t* __restrict__ token_slots, int topk,
+                                                          int num_slots, uint8_t* __restrict__ ws, WsLayout L) {
+  __shared__ int s_warp[32];
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+  const int row = blockIdx.x;
+  const int32_t* src = token_slots + static_cast<size_t>(row) * topk;
+  int* dst = reinterpret_cast<int*>(ws + L.sp_slots) + static_cast<size_t>(row) * topk;
+  int base = 0;
+  for (int c0 = 0; c0 < topk; c0 += blockDim.x) {
+    const int k = c0 + static_cast<int>(threadIdx.x);
+    const int v = k < topk ? src[k] : -1;
+    const bool ok = v >= 0 && v < num_slots;
+    if (k < topk && !ok && v != -1) set_status(&hdr->status, MLA_STATUS_BAD_INDEX);
+    int total = 0;
+    const int pos = block_exclusive_scan(ok ? 1 : 0, s_warp, &total);
+    if (ok) dst[base + pos] = v;
+    base += total;
+  }
+  if (threadIdx.x == 0) reinterpret_cast<int*>(ws + L.sp_lens)[row] = base;
+}
+
 }  // namespace
+
+cudaError_t launch_sparse_prep(const int32_t* token_slots, int rows, int topk, int num_slots, void* ws,
+                               const WsLayout& L, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  sparse_prep_kernel<<<rows, 256, 0, stream>>>(token_slots, topk, num_slots, static_cast<uint8_t*>(ws), L);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_pages, int pairs_per_group,
                         void* ws, const WsLayout& L, cudaStream_t stream) {

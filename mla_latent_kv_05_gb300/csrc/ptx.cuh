@@ -184,6 +184,16 @@ __device__ __forceinline__ void bulk_copy_s2s(uint32_t dst, uint32_t src, uint32
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), cached
+// in L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued before has landed;
+// the barrier's expected count includes this arrival (no increment).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
 // Prefetch a contiguous global range (16-byte aligned, multiple of 16 B) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");

@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_expected_entry_points():
     names = declared_functions()
     for n in ("mla_decode_bf16", "mla_decode_fp8", "mla_combine_splits", "mla_workspace_size",
-              "mla_get_status", "mla_status_string"):
+              "mla_get_status", "mla_status_string", "mla_decode_sparse_bf16", "mla_workspace_size_sparse"):
         assert n in names
 
 
@@ -63,3 +63,20 @@ def test_host_validation_without_gpu(lib):
         rc = lib.mla_decode_bf16(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(bad_scale),
                                  fake, fake, fake, 1 << 30, z)
         assert rc == -1
+
+
+def test_sparse_host_validation_without_gpu(lib):
+    z = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+    n = ctypes.c_size_t(0)
+    assert lib.mla_workspace_size_sparse(1, 1, 0, 128, 64, ctypes.byref(n)) == -1        # topk = 0
+    assert lib.mla_workspace_size_sparse(1, 1, 1 << 15, 128, 64, ctypes.byref(n)) == -2  # topk > 16384
+    assert lib.mla_workspace_size_sparse(1, 1, 64, 64, 64, ctypes.byref(n)) == -2        # num_heads != 128
+    rc = lib.mla_decode_sparse_bf16(z, z, z, z, 1, 1, 64, 128, 8, 64, ctypes.c_float(0.1), z, z, z, 0, z)
+    assert rc == -1
+    rc = lib.mla_decode_sparse_bf16(fake, fake, fake, fake, 1, 1, 64, 128, 8, 32, ctypes.c_float(0.1),
+                                    fake, fake, fake, 1 << 30, z)
+    assert rc == -2                                                                   # page_size != 64
+    rc = lib.mla_decode_sparse_bf16(fake, fake, fake, fake, 1, 1, 64, 128, 8, 64, ctypes.c_float(float("inf")),
+                                    fake, fake, fake, 1 << 30, z)
+    assert rc == -1
