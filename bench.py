@@ -11,7 +11,8 @@ stream), an end-to-end number through the public API with host buffers, the
 float64 oracle timed on the host cores on a bounded sample, and the SM
 clocks sampled during the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..6]
+  (workloads 1..5: the dense configurations; 6: sparse top-2048 decode)
   python bench.py --impl reference ...   # the oracle arm (host cores)
 """
 from __future__ import annotations
@@ -210,19 +211,51 @@ def oracle_sample(inp, budget_s: float, max_tokens_per_piece: int = 4096):
     return tokens, dt, f"{pieces} (row, all queries) attentions of <= {max_tokens_per_piece} tokens, 128 heads"
 
 
+def oracle_sample_sparse(sp, budget_s: float):
+    """The oracle on a bounded sample of a sparse workload: whole query rows
+    (all listed tokens) in order until `budget_s` elapses."""
+    from oracle import mla_oracle
+    d = sp.dense
+    flat = d.kv_cache.view(-1, d.kv_cache.shape[-1])
+    tokens, pieces = 0, 0
+    t0 = time.perf_counter()
+    r = 0
+    while time.perf_counter() - t0 < budget_s:
+        b, i = divmod(r % (d.batch * d.sq), d.sq)
+        s = sp.token_slots[b, i]
+        s = s[s >= 0].long()
+        rows = flat[s].double().numpy().reshape(1, -1, flat.shape[-1])
+        g = mla_oracle.sparse_gather_rows(rows, np.arange(s.numel()))
+        mla_oracle.attend_latent(d.q_absorbed[b, i].double().numpy(), d.q_rope[b, i].double().numpy(), g, d.scale)
+        tokens += int(s.numel())
+        pieces += 1
+        r += 1
+    dt = time.perf_counter() - t0
+    return tokens, dt, f"{pieces} query rows with all their listed tokens (<= {sp.topk}), 128 heads"
+
+
+def load_problem(workload: int):
+    """(dense inputs, sparse inputs or None) of a workload."""
+    if workload in gen.SPARSE_WORKLOADS:
+        sp = gen.make_sparse_workload(workload)
+        return sp.dense, sp
+    return gen.make_workload(workload), None
+
+
 def run_reference(args):
     world, rank, local = dist_setup()
     if rank != 0:
         return 0
-    inp = gen.make_workload(args.workload)
-    cfg = workload_config(args.workload, inp)
+    inp, sp = load_problem(args.workload)
+    cfg = workload_config(args.workload, inp, sp)
     per_step = 0.01
+    sample = (lambda b: oracle_sample_sparse(sp, b)) if sp is not None else (lambda b: oracle_sample(inp, b))
     for _ in range(args.warmup):
-        oracle_sample(inp, per_step)
+        sample(per_step)
     tot_tok, tot_s = 0, 0.0
     desc = ""
     for _ in range(args.steps):
-        t, s, desc = oracle_sample(inp, per_step)
+        t, s, desc = sample(per_step)
         tot_tok += t
         tot_s += s
     value = tot_tok / tot_s
@@ -240,7 +273,16 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- GPU arm
-def workload_config(workload: int, inp) -> dict:
+def workload_config(workload: int, inp, sp=None) -> dict:
+    if sp is not None:
+        c = gen.sparse_counts(sp)
+        cache_bytes = inp.kv_cache.numel() * inp.kv_cache.element_size()
+        return {"workload": gen.SPARSE_WORKLOADS[workload]["name"], "batch": inp.batch, "sq": inp.sq,
+                "heads": int(inp.q_absorbed.shape[2]), "kv_dtype": inp.kv_dtype, "page_size": 64,
+                "topk": sp.topk, "kv_tokens": c["kv_tokens"], "seed": gen.seed_for(workload),
+                "l2": ("inputs larger than L2 (listed rows %.0f MB > 129 MB; KV cache %.0f MB)"
+                       % (c["kv_bytes"] / 1e6, cache_bytes / 1e6)) if c["kv_bytes"] > L2_BYTES
+                else "L2 flushed between steps"}
     c = gen.workload_counts(inp)
     return {"workload": gen.WORKLOADS[workload]["name"], "batch": inp.batch, "sq": inp.sq,
             "heads": int(inp.q_absorbed.shape[2]), "kv_dtype": inp.kv_dtype, "page_size": 64,
@@ -254,24 +296,40 @@ def run_ours(args):
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    inp = gen.make_workload(args.workload)
-    counts = gen.workload_counts(inp)
-    decode = binding.mla_decode_bf16 if inp.kv_dtype == "bf16" else binding.mla_decode_fp8
+    inp, sp = load_problem(args.workload)
     q = inp.q_absorbed.to(dev)
     qr = inp.q_rope.to(dev)
     kv = inp.kv_cache.to(dev)
-    bt = inp.block_table.to(dev)
-    sl = inp.seq_lens.to(dev)
     out = torch.empty((inp.batch, inp.sq, 128, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((inp.batch, inp.sq, 128), dtype=torch.float32, device=dev)
-    ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
     stream = torch.cuda.current_stream(dev)
+    if sp is not None:
+        # sparse top-k decode: four launches per call (compaction, planner,
+        # attention, merge); the per-step inputs are q, q_rope and the lists
+        counts = gen.sparse_counts(sp)
+        slots = sp.token_slots.to(dev)
+        ws = binding.alloc_workspace_sparse(inp.batch, inp.sq, sp.topk, dev)
+        launches = 4
+        uploads = [(sp.token_slots.pin_memory(), slots)]
+
+        def step():
+            binding.mla_decode_sparse_bf16(q, qr, kv, slots, inp.scale, out=out, lse=lse, workspace=ws)
+    else:
+        counts = gen.workload_counts(inp)
+        decode = binding.mla_decode_bf16 if inp.kv_dtype == "bf16" else binding.mla_decode_fp8
+        bt = inp.block_table.to(dev)
+        sl = inp.seq_lens.to(dev)
+        ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
+        # planner, attention, merge (FP8: the exact pass after the f16 pass is
+        # a fourth launch, which returns at once unless needed)
+        launches = 3 if inp.kv_dtype == "bf16" else 4
+        uploads = [(inp.block_table.pin_memory(), bt), (inp.seq_lens.pin_memory(), sl)]
+
+        def step():
+            decode(q, qr, kv, bt, sl, inp.scale, out=out, lse=lse, workspace=ws)
     flush = None
     if counts["kv_bytes"] <= L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        decode(q, qr, kv, bt, sl, inp.scale, out=out, lse=lse, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -348,8 +406,6 @@ def run_ours(args):
     # ---- end to end through the public API with pinned host buffers
     hq = inp.q_absorbed.pin_memory()
     hqr = inp.q_rope.pin_memory()
-    hbt = inp.block_table.pin_memory()
-    hsl = inp.seq_lens.pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     e2e_steps = max(3, min(args.steps, 50))
@@ -357,8 +413,8 @@ def run_ours(args):
     def e2e_step():
         q.copy_(hq, non_blocking=True)
         qr.copy_(hqr, non_blocking=True)
-        bt.copy_(hbt, non_blocking=True)
-        sl.copy_(hsl, non_blocking=True)
+        for h, d in uploads:
+            d.copy_(h, non_blocking=True)
         step()
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
@@ -376,24 +432,25 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = sum_over_ranks(float(counts["kv_tokens"] * e2e_steps), world, dev) / (e2e_ms / 1000.0)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hqr, hbt, hsl))
+    h2d = sum(t.numel() * t.element_size() for t in [hq, hqr] + [h for h, _ in uploads])
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
     line = {
         "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_call": ms_per_step * 1000.0,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": inp.kv_dtype,
-        "data": "synthetic", "config": workload_config(args.workload, inp),
+        "data": "synthetic", "config": workload_config(args.workload, inp, sp),
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "KV-tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "q, q_rope, block_table, seq_lens uploaded and out, lse read back every step; "
-                        "the KV cache stays resident in HBM"},
-        "gpu_launches": 3 * args.steps,
+                "note": ("q, q_rope, the slot lists" if sp is not None else "q, q_rope, block_table, seq_lens")
+                        + " uploaded and out, lse read back every step; the KV cache stays resident in HBM"},
+        "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tok, sec, desc = oracle_sample(inp, args.cpu_seconds)
+        tok, sec, desc = (oracle_sample_sparse(sp, args.cpu_seconds) if sp is not None
+                          else oracle_sample(inp, args.cpu_seconds))
         line["cpu_baseline"] = {"value": tok / sec, "unit": "KV-tokens/s", "cores": _CORES, "kind": "oracle",
                                 "sample": f"{desc}; {sec:.1f}s of host work"}
     if rank == 0:
@@ -409,7 +466,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=3, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(gen.WORKLOADS) + sorted(gen.SPARSE_WORKLOADS))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
