@@ -527,25 +527,41 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const int my_slot = lane < n_rows ? __ldg(slots + r0 + lane) : 0;
         const int c = lane >> 3, q = lane & 7;                  // chunk (of four) and 16-byte piece of a lane
         if (rank == 1) {
-          const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);
+          // A part: chunks 0..3 of a row are 32 pieces, lane L taking piece
+          // L (chunk L/8, piece L%8) of every row; chunk 4 of four rows at a
+          // time are 32 pieces, lane L taking piece L%8 of row L/8 of the
+          // four.  B part: chunks 5..8, lane L taking piece L of every row.
+          const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot) +
+                                 static_cast<uint32_t>(gw) * (4 * 5 * kAtom);     // row group 4 gw
           if (!wait_warp<false>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+          const uint8_t* asrc = p.kv_bf16 + lane * 16;
+#pragma unroll 4
           for (int i = 0; i < n_rows; ++i) {
             const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-            const uint8_t* src = p.kv_bf16 + static_cast<size_t>(slot) * (kRow * 2);
-            const int r = gw * kHalf + i;                        // row of the tile
-            const uint32_t row = tbase + static_cast<uint32_t>(r >> 3) * (5 * kAtom) + (r & 7) * 128;
-            ptx::cp_async_16(row + c * kAtom + ((q ^ (r & 7)) << 4), src + c * 128 + q * 16);
-            if (lane < 8) ptx::cp_async_16(row + 4 * kAtom + ((q ^ (r & 7)) << 4), src + 4 * 128 + q * 16);
+            ptx::cp_async_16(tbase + static_cast<uint32_t>(i >> 3) * (5 * kAtom) + c * kAtom + (i & 7) * 128 +
+                                 ((q ^ (i & 7)) << 4),
+                             asrc + static_cast<size_t>(slot) * (kRow * 2));
+          }
+          const uint8_t* a4src = p.kv_bf16 + 4 * 128 + q * 16;
+#pragma unroll 2
+          for (int g = 0; 4 * g < n_rows; ++g) {
+            const int row = 4 * g + c;                          // c = lane / 8 < 4
+            const int slot = __shfl_sync(0xffffffffu, my_slot, row);
+            if (row < n_rows)
+              ptx::cp_async_16(tbase + static_cast<uint32_t>(row >> 3) * (5 * kAtom) + 4 * kAtom + (row & 7) * 128 +
+                                   ((q ^ (row & 7)) << 4),
+                               a4src + static_cast<size_t>(slot) * (kRow * 2));
           }
           ptx::cp_async_arrive_noinc(BAR(KFULL + kb));
           if (!wait_warp<false>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+          const uint32_t bbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot) + static_cast<uint32_t>(TH) * kKA +
+                                 static_cast<uint32_t>(gw) * (4 * 4 * kAtom) + c * kAtom;
+          const uint8_t* bsrc = p.kv_bf16 + (5 + c) * 128 + q * 16;
+#pragma unroll 4
           for (int i = 0; i < n_rows; ++i) {
             const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-            const uint8_t* src = p.kv_bf16 + static_cast<size_t>(slot) * (kRow * 2);
-            const int r = gw * kHalf + i;
-            const uint32_t row = tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(r >> 3) * (4 * kAtom) +
-                                 (r & 7) * 128;
-            ptx::cp_async_16(row + c * kAtom + ((q ^ (r & 7)) << 4), src + (5 + c) * 128 + q * 16);
+            ptx::cp_async_16(bbase + static_cast<uint32_t>(i >> 3) * (4 * kAtom) + (i & 7) * 128 + ((q ^ (i & 7)) << 4),
+                             bsrc + static_cast<size_t>(slot) * (kRow * 2));
           }
           ptx::cp_async_arrive_noinc(BAR(KFULLB + kb));
           kb ^= 1;
@@ -556,13 +572,15 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             uint32_t vp = vphase;
             if (v >= kVSlots) { v -= kVSlots; vp ^= 1u; }
             if (!wait_warp<false>(BAR(VEMPTY + v), vp ^ 1u, hdr)) { ok = false; break; }
-            const uint32_t vbase = sbase + static_cast<uint32_t>(v) * kVSlot;
+            const uint32_t vbase = sbase + static_cast<uint32_t>(v) * kVSlot + c * kAtom;
+            const uint8_t* vsrc = p.kv_bf16 + lane * 16;
+#pragma unroll 4
             for (int i = 0; i < n_rows; ++i) {
               const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-              const uint8_t* src = p.kv_bf16 + static_cast<size_t>(slot) * (kRow * 2);
-              const uint32_t row = vbase + static_cast<uint32_t>(i >> 3) * kVGroup + (i & 7) * 128;
-              ptx::cp_async_16(row + c * kAtom + ((q ^ (i & 7)) << 4), src + c * 128 + q * 16);
-              ptx::cp_async_16(row + (c + 4) * kAtom + ((q ^ (i & 7)) << 4), src + (c + 4) * 128 + q * 16);
+              const uint8_t* src = vsrc + static_cast<size_t>(slot) * (kRow * 2);
+              const uint32_t dst = vbase + static_cast<uint32_t>(i >> 3) * kVGroup + (i & 7) * 128 + ((q ^ (i & 7)) << 4);
+              ptx::cp_async_16(dst, src);
+              ptx::cp_async_16(dst + 4 * kAtom, src + 512);
             }
             ptx::cp_async_arrive_noinc(BAR(VFULL + v));
           }
