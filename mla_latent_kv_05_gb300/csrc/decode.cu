@@ -49,6 +49,11 @@
 // Moving dequantised rows between the two SMs would cost more than the
 // second dequant: traffic inside a cluster runs at about 42 GB/s per pair.
 //
+// Sparse top-k decode (mode 3) is the bf16 kernel with the copies done by
+// three warps per SM that gather listed cache rows with 16-byte cp.async
+// into the same layouts (TMA cannot gather 1152-byte rows into the swizzled
+// operand layout at a useful rate).
+//
 // Lazy rescaling: rank 1 keeps a per-head reference max m_ref (raw score
 // units) and moves it only when a tile's max exceeds it by more than 16 in
 // log2 units, so P <= 2^16 and O is rescaled only on those tiles; the

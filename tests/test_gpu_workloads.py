@@ -33,3 +33,26 @@ def test_workload_full_size(cuda_device, workload):
     rows = sampled_rows(inp)
     ref_out, ref_lse = oracle(inp, rows)
     assert_close(out, lse, ref_out, ref_lse, rows)
+
+
+def test_sparse_workload_full_size(cuda_device):
+    # workload 6 (sparse top-2048, 64 rows over 32K contexts) through the
+    # public sparse entry point, checked on sampled query rows
+    from test_gpu_sparse import run_sparse
+    from oracle import mla_oracle
+    sp = gen.make_sparse_workload(6)
+    out, lse, st = run_sparse(sp)
+    assert st == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    d = sp.dense
+    flat = d.kv_cache.view(-1, 576)
+    rng = np.random.default_rng(6)
+    for b in sorted({0, d.batch - 1, *rng.integers(d.batch, size=3).tolist()}):
+        s = sp.token_slots[b, 0]
+        s = s[s >= 0].long()
+        rows = flat[s].double().numpy()
+        ro, rl = mla_oracle.attend_latent(d.q_absorbed[b, 0].double().numpy(), d.q_rope[b, 0].double().numpy(),
+                                          rows, d.scale)
+        got = out[b, 0].double().cpu().numpy()
+        assert np.abs(got - ro).max() <= 1e-2 * np.abs(ro).max(), b
+        assert np.abs(lse[b, 0].double().cpu().numpy() - rl).max() <= 1e-3, b
