@@ -158,6 +158,18 @@ int mla_decode_sparse_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,
                            uint16_t* out, float* lse, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* Up-projection of latent attention outputs through W^UV ("DeepSeek R1
+ * Architecture & Deployment Guide", section 1.1: the value up-projection is
+ * folded out of the attention, which returns the 512-value latent output
+ * per head): out[r][h][:] = W_uv[h] . latent[r][h][:], i.e. per head the GEMM
+ * [rows x 512] . [512 x d_v].  latent [rows, 128, 512] bf16 (the decode's
+ * out), w_uv [128, d_v, 512] bf16, out [rows, 128, d_v] bf16 (fp32
+ * accumulation, rounded to nearest).  num_heads must be 128 and d_v 128.
+ * workspace: at least 256 bytes, 256-byte aligned; it receives the status
+ * word (read with mla_get_status; the decode's workspace may be reused). */
+int mla_up_project_wuv(const uint16_t* latent, const uint16_t* w_uv, int rows, int num_heads, int d_v,
+                       uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Merge split-KV partial results (attention over disjoint token sets):
  *   L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * partial_out_s,
  *   lse = L.

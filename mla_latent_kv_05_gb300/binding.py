@@ -35,6 +35,7 @@ SIGNATURES = {
     "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_decode_sparse_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
+    "mla_up_project_wuv": (_I, [_P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
     "mla_combine_splits": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
     "mla_get_status": (_I, [_P, _P]),
     "mla_profile_next_decode": (_I, [_P, _P]),
@@ -243,6 +244,30 @@ def mla_decode_sparse_bf16(q_absorbed, q_rope, kv_cache, token_slots, scale, out
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_sparse_bf16")
     return out, lse
+
+
+def mla_up_project_wuv(latent, w_uv, out=None, workspace=None, stream=None):
+    """out[r, h] = w_uv[h] @ latent[r, h]: latent [..., 128, 512] bf16 (the
+    decode's output), w_uv [128, 128, 512] bf16 -> [..., 128, 128] bf16."""
+    lead = tuple(latent.shape[:-2])
+    _check(latent, "latent", torch.bfloat16)
+    if tuple(latent.shape[-2:]) != (128, 512):
+        raise ValueError("latent must be [..., 128, 512]")
+    _check(w_uv, "w_uv", torch.bfloat16, (128, 128, 512))
+    rows = 1
+    for x in lead:
+        rows *= int(x)
+    if out is None:
+        out = torch.empty(lead + (128, 128), dtype=torch.bfloat16, device=latent.device)
+    _check(out, "out", torch.bfloat16, lead + (128, 128))
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=latent.device)
+    _check(workspace, "workspace", torch.uint8)
+    rc = load().mla_up_project_wuv(_ptr(latent), _ptr(w_uv), rows, 128, 128, _ptr(out), _ptr(workspace),
+                                   ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_up_project_wuv")
+    return out
 
 
 def mla_combine_splits(partial_out, partial_lse, split_indptr, out=None, lse=None, stream=None):

@@ -222,6 +222,24 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
 
 extern "C" {
 
+int mla_up_project_wuv(const uint16_t* latent, const uint16_t* w_uv, int rows, int num_heads, int d_v,
+                       uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!latent || !w_uv || !out || !workspace || rows < 0) return MLA_ERR_INVALID_ARG;
+  if (num_heads != kHeads || d_v != 128) return MLA_ERR_UNSUPPORTED;
+  if (rows > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (!aligned(latent, 16) || !aligned(w_uv, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < sizeof(PlanHeader)) return MLA_ERR_WORKSPACE;
+  if (rows == 0) return MLA_OK;
+  auto fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + offsetof(PlanHeader, abort_flag), 0, sizeof(int), st) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  return launch_wuv(fn, latent, w_uv, rows, out, workspace, st) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int mla_workspace_size_sparse(int batch, int sq, int topk, int num_heads, int page_size, size_t* bytes) {
   if (!bytes || batch < 0 || sq <= 0 || topk <= 0) return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || page_size != kPage || topk > kMaxTopk) return MLA_ERR_UNSUPPORTED;

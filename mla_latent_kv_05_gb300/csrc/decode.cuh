@@ -1,6 +1,7 @@
 // Parameters and host launchers of the MLA decode kernels.
 #pragma once
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -40,6 +41,9 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cuda
 // with one query each).
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 int decode_max_pairs();
+// W^UV up-projection of latent outputs (see wuv.cu).
+cudaError_t launch_wuv(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* o, const void* w, int rows, void* out,
+                       void* hdr, cudaStream_t stream);
 cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int max_rows, __nv_bfloat16* out, float* lse,
                                 bool pdl, cudaStream_t stream);
 cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,
