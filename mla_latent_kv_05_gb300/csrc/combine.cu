@@ -13,19 +13,29 @@ namespace mla {
 
 namespace {
 
-__device__ __forceinline__ void load4(const float* src, int i, float* x) {
-  const float4 v = __ldcs(reinterpret_cast<const float4*>(src) + i);
-  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+// Eight consecutive values of a partial row, as fp32: element offset e
+// (a multiple of 8), 16-byte loads that bypass L1 (each partial is read once).
+__device__ __forceinline__ void load8(const float* src, int e, float* x) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(src + e));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(src + e + 4));
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
-__device__ __forceinline__ void load4(const __nv_bfloat16* src, int i, float* x) {
-  const uint2 v = __ldcs(reinterpret_cast<const uint2*>(src) + i);
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+__device__ __forceinline__ void load8(const __nv_bfloat16* src, int e, float* x) {
+  const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src + e));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
 }
 
 // grid (rows, 128 / 8): one warp per (row, head); lane holds values
-// 4(32q + lane) .. +3 for q = 0..3.
+// [8 lane, 8 lane + 8) and [256 + 8 lane, 256 + 8 lane + 8).  Each lane reads
+// one part's lse (parts beyond 32 loop); the weights reach the other lanes by
+// shuffles, and the parts' values are loaded four parts at a time so their
+// loads overlap.
 template <typename TP>
 __global__ void __launch_bounds__(256) combine_kernel(const TP* __restrict__ part_out,
                                                       const float* __restrict__ part_lse,
@@ -45,7 +55,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const TP* __restrict__ par
   const int row = row_index ? row_index[k] : k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
-  // each lane reads one part's lse (parts beyond 32 loop), then a warp max / sum
   float L = -INFINITY;
   for (int s = lane; s < count; s += 32) L = fmaxf(L, part_lse[static_cast<size_t>(start + s) * kHeads + h]);
 #pragma unroll
@@ -55,28 +64,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const TP* __restrict__ par
   for (int e = 0; e < 16; ++e) acc[e] = 0.f;
   float sum = 0.f;
   if (L != -INFINITY) {
-    for (int s = 0; s < count; ++s) {
-      const float v = part_lse[static_cast<size_t>(start + s) * kHeads + h];
-      const float wgt = v == -INFINITY ? 0.f : __expf(v - L);
-      sum += wgt;
-      const TP* src = part_out + (static_cast<size_t>(start + s) * kHeads + h) * kDc;
-      float x[16];
+    for (int s0 = 0; s0 < count; s0 += 32) {
+      // this lane's part weight for parts s0 .. s0 + 31
+      const int sl = s0 + lane;
+      const float v = sl < count ? part_lse[static_cast<size_t>(start + sl) * kHeads + h] : -INFINITY;
+      const float wl = v == -INFINITY ? 0.f : __expf(v - L);
+      const int n = min(32, count - s0);
+      for (int j0 = 0; j0 < n; j0 += 4) {
+        float x[4][16], wgt[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) load4(src, q * 32 + lane, x + 4 * q);
+        for (int u = 0; u < 4; ++u) {
+          wgt[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
+          if (j0 + u < n) {
+            const TP* src = part_out + (static_cast<size_t>(start + s0 + j0 + u) * kHeads + h) * kDc;
+            load8(src, 8 * lane, x[u]);
+            load8(src, 256 + 8 * lane, x[u] + 8);
+          } else {
+            wgt[u] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] += wgt * x[e];
+            for (int e = 0; e < 16; ++e) x[u][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          sum += wgt[u];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] += wgt[u] * x[u][e];
+        }
+      }
     }
   }
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   __nv_bfloat16* dst = out + (static_cast<size_t>(row) * kHeads + h) * kDc;
+  uint32_t o[8];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * q] * inv, acc[4 * q + 1] * inv);
-    __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&a);
-    v.y = *reinterpret_cast<uint32_t*>(&b);
-    reinterpret_cast<uint2*>(dst)[q * 32 + lane] = v;
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * half + 2 * q] * inv, acc[8 * half + 2 * q + 1] * inv);
+      o[q] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(dst + 256 * half + 8 * lane) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (lane == 0) lse[static_cast<size_t>(row) * kHeads + h] = sum > 0.f ? L + logf(sum) : -INFINITY;
 }
