@@ -53,13 +53,21 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
 
 
+# The sources the recorded DRAM counters depend on: the attention kernel and
+# the headers it includes, and the planner (its partition sets the split
+# partials the kernel writes).  The merge, W^UV and API files are not among
+# them.
+KERNEL_SOURCES = ("decode.cu", "decode.cuh", "common.cuh", "ptx.cuh", "plan.cu")
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources' code: line comments and blank lines are
-    dropped, so a comment-only edit keeps recorded counters valid."""
+    """Hash of the attention kernel's and planner's code: line comments and
+    blank lines are dropped, so a comment-only edit keeps recorded counters
+    valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_05_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name in KERNEL_SOURCES:
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 lines = []
                 for line in f:
