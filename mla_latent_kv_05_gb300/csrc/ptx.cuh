@@ -39,13 +39,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};"
-               :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.b32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
-}
 
 // Asynchronous stores into another CTA's shared memory: the bytes are counted
 // (complete_tx) on the mbarrier `bar` of that CTA when they land, so the
@@ -91,9 +84,6 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async_cta() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -138,13 +128,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
-// 2-D tiled load, completion counted in bytes on `bar` (this CTA).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,
-                                            int32_t x, int32_t y, uint64_t policy) {
-  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-               " [%0], [%1, {%3, %4}], [%2], %5;"
-               :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "l"(policy) : "memory");
-}
 // 3-D tiled load (x, y, z coordinates), completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar,
                                             int32_t x, int32_t y, int32_t z, uint64_t policy) {
@@ -175,15 +158,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                " [%0], [%1], %2, [%3], %4;"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
-// Bulk copy from this CTA's shared memory (src, a shared::cta address) into
-// the shared memory of a CTA of the cluster (dst, a shared::cluster address
-// from mapa); the bytes are counted on `bar`, an mbarrier in the destination
-// CTA (also a shared::cluster address).  Both addresses 16-byte aligned,
-// size a multiple of 16.
-__device__ __forceinline__ void bulk_copy_s2s(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               :: "r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
-}
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned), cached
 // in L2 only.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
@@ -206,11 +180,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ uint64_t policy_evict_normal() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
