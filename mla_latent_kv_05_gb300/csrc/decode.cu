@@ -1130,7 +1130,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const bool split = slot_base[sg.b] >= 0;
         const int slot = split ? group * spq + slot_base[sg.b] + (pair_rank[pl] - pair_rank[first_pair[sg.b]]) : -1;
         const float lse_v = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -INFINITY;
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;   // correctly rounded, as 1/l
         if (split) part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
         else p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
         if (!wait_warp<true>(BAR(MBEMPTY + ms), mphase ^ 1u, hdr)) { ok = false; break; }
