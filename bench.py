@@ -11,8 +11,9 @@ stream), an end-to-end number through the public API with host buffers, the
 float64 oracle timed on the host cores on a bounded sample, and the SM
 clocks sampled during the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..6]
-  (workloads 1..5: the dense configurations; 6: sparse top-2048 decode)
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..7]
+  (workloads 1..5: the dense configurations; 6: sparse top-2048 decode;
+  7: the FP4 cache at the FP8 workload's shape)
   python bench.py --impl reference ...   # the oracle arm (host cores)
 """
 from __future__ import annotations
@@ -193,7 +194,7 @@ def oracle_sample(inp, budget_s: float, max_tokens_per_piece: int = 4096):
     at most `max_tokens_per_piece` tokens, until `budget_s` elapses.
     Returns (KV tokens processed, seconds, description)."""
     from oracle import mla_oracle
-    raw = inp.kv_cache if inp.kv_dtype == "fp8" else inp.kv_cache
+    raw = inp.kv_cache
     qa = inp.q_absorbed
     qr = inp.q_rope
     tokens = 0
@@ -206,7 +207,7 @@ def oracle_sample(inp, budget_s: float, max_tokens_per_piece: int = 4096):
         if n > 0:
             pages = inp.block_table[bb, : (n + 63) // 64].long()
             sub = raw[pages]
-            rows = mla_oracle.cache_rows(sub.numpy() if inp.kv_dtype == "fp8" else sub.double().numpy(),
+            rows = mla_oracle.cache_rows(sub.double().numpy() if inp.kv_dtype == "bf16" else sub.numpy(),
                                          inp.kv_dtype)
             local_bt = np.arange(len(pages))
             g = mla_oracle.gather_rows(rows, local_bt, n)
@@ -327,13 +328,14 @@ def run_ours(args):
             call(q, qr, [slots], out, lse)
     else:
         counts = gen.workload_counts(inp)
-        decode = binding.mla_decode_bf16 if inp.kv_dtype == "bf16" else binding.mla_decode_fp8
+        decode = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8,
+                  "fp4": binding.mla_decode_fp4}[inp.kv_dtype]
         bt = inp.block_table.to(dev)
         sl = inp.seq_lens.to(dev)
         ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
         # planner, attention, merge (FP8: the exact pass after the f16 pass is
         # a fourth launch, which returns at once unless needed)
-        launches = 3 if inp.kv_dtype == "bf16" else 4
+        launches = 4 if inp.kv_dtype == "fp8" else 3
         uploads = [(inp.block_table.pin_memory(), bt), (inp.seq_lens.pin_memory(), sl)]
 
         def call(qb, qrb, extra, outb, lseb):

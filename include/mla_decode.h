@@ -138,6 +138,25 @@ int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope,
                    float softmax_scale, uint16_t* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Same over an FP4 cache [num_pages, 64, 324] (uint8).  The "DeepSeek-R1"
+ * model record (engine kernel constraint (2)) gives only the size of the
+ * FP4 variant, 288 bytes per token for a 512-value row; the reading taken
+ * is e2m1 codes for every value (two per byte, value 2k in the low nibble
+ * of byte k) followed by one e8m0 scale per 16 values, which is 256 + 32 =
+ * 288 bytes for 512 values and 288 + 36 = 324 bytes for this 576-value row:
+ *   v[k] = e2m1(nibble k) * 2^(byte[288 + k/16] - 127),
+ * e2m1 = OCP MX FP4: sign, 2 exponent bits (bias 1), 1 mantissa bit.
+ * The values are exact in bf16 for scale bytes in [0, 252] (255 is NaN;
+ * 253 and 254 overflow) and are attended with bf16 operands, as the bf16
+ * path does.  kv_cache must be 16-byte aligned.  Arguments, layouts,
+ * results and errors are otherwise those of mla_decode_bf16. */
+int mla_decode_fp4(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                   const uint8_t* kv_cache, const int32_t* block_table,
+                   const int32_t* seq_lens, int batch, int sq, int num_heads,
+                   int num_pages, int page_size, int max_pages,
+                   float softmax_scale, uint16_t* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Sparse top-k decode ("DeepSeek-V3.2" model record: the sparse attention
  * indexer, index_topk 2048, selects the candidate tokens each query attends
  * over; the latent rows stay cached per token).  Query row (b, i) attends

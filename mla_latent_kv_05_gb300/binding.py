@@ -32,6 +32,8 @@ SIGNATURES = {
                                      _P]),
     "mla_decode_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                             ctypes.c_size_t, _P]),
+    "mla_decode_fp4": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                            ctypes.c_size_t, _P]),
     "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_decode_sparse_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
@@ -195,6 +197,15 @@ def mla_decode_fp8(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, o
     576 e4m3 codes then 18 e8m0 scales); returns (out, lse)."""
     return _decode("mla_decode_fp8", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
                    workspace, stream, torch.uint8, 594)
+
+
+def mla_decode_fp4(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out=None, lse=None,
+                   workspace=None, stream=None):
+    """MLA decode over an FP4 latent cache [num_pages, 64, 324] (uint8 rows:
+    576 e2m1 codes, two per byte with the even value in the low nibble, then
+    36 e8m0 scales, one per 16 values); returns (out, lse)."""
+    return _decode("mla_decode_fp4", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
+                   workspace, stream, torch.uint8, 324)
 
 
 def mla_workspace_size_sparse(batch: int, sq: int, topk: int, num_heads: int = 128, page_size: int = 64) -> int:

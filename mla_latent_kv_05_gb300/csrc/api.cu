@@ -70,7 +70,9 @@ int validate_common(const void* q_absorbed, const void* q_rope, const void* kv_c
   return MLA_OK;
 }
 
-int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache,
+enum class CacheKind { kBf16, kFp8, kFp4 };
+
+int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache,
                const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads, int num_pages,
                int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse, void* workspace,
                size_t workspace_bytes, void* stream_ptr) {
@@ -87,7 +89,8 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
 
   // half pages: chunks 0..4 and 5..8 (score SM), the 8 latent chunks (value SM)
   CUtensorMap tmap_k, tmap_kb, tmap_v;
-  if (!fp8) {
+  const bool quant = kind != CacheKind::kBf16;
+  if (!quant) {
     st = make_cache_tmap(&tmap_k, kv_cache, num_pages, 5);
     if (st == MLA_OK) st = make_cache_tmap(&tmap_kb, kv_cache, num_pages, 4);
     if (st == MLA_OK) st = make_cache_tmap(&tmap_v, kv_cache, num_pages, 8);
@@ -98,8 +101,8 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   DecodeParams p;
   p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
   p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
-  p.kv_fp8 = fp8 ? static_cast<const uint8_t*>(kv_cache) : nullptr;
-  p.kv_bf16 = fp8 ? nullptr : static_cast<const uint8_t*>(kv_cache);
+  p.kv_quant = quant ? static_cast<const uint8_t*>(kv_cache) : nullptr;
+  p.kv_bf16 = quant ? nullptr : static_cast<const uint8_t*>(kv_cache);
   p.sp_slots = nullptr;
   p.topk = 0;
   p.block_table = block_table;
@@ -122,8 +125,9 @@ int run_decode(bool fp8, const uint16_t* q_absorbed, const uint16_t* q_rope, con
   g_prof_before = g_prof_after = nullptr;
   const bool pdl = ev0 == nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  const cudaError_t le = fp8 ? launch_decode_fp8(p, ppg * sq, pdl, stream)
-                             : launch_decode_bf16(tmap_k, tmap_kb, tmap_v, p, ppg * sq, pdl, stream);
+  const cudaError_t le = kind == CacheKind::kFp8   ? launch_decode_fp8(p, ppg * sq, pdl, stream)
+                         : kind == CacheKind::kFp4 ? launch_decode_fp4(p, ppg * sq, pdl, stream)
+                                                   : launch_decode_bf16(tmap_k, tmap_kb, tmap_v, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -272,7 +276,7 @@ int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope, const ui
                     const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
                     int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  return run_decode(false, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+  return run_decode(CacheKind::kBf16, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
                     page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
@@ -294,7 +298,7 @@ int mla_decode_bf16_noalloc(const uint16_t* q_absorbed, const uint16_t* q_rope, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the status word and the abort flag must start at zero for this call
   if (cudaMemsetAsync(scratch, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
-  st = run_decode(false, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+  st = run_decode(CacheKind::kBf16, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
                   page_size, max_pages, softmax_scale, out, lse, scratch, kStaticScratchBytes, stream);
   if (st != MLA_OK) return st;
   if (device_status &&
@@ -307,8 +311,16 @@ int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope, const uin
                    const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
                    int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  return run_decode(true, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
+  return run_decode(CacheKind::kFp8, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
                     page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_fp4(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint8_t* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
+                   int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  return run_decode(CacheKind::kFp4, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads,
+                    num_pages, page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 int mla_combine_splits(const float* partial_out, const float* partial_lse, const int32_t* split_indptr, int rows,

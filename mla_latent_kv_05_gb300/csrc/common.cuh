@@ -16,6 +16,8 @@ constexpr int kDr = 64;             // decoupled RoPE key
 constexpr int kRow = kDc + kDr;     // 576 values per cached token
 constexpr int kPage = 64;           // tokens per page (= tokens per KV tile)
 constexpr int kFp8Row = kRow + kRow / 32;   // 594 bytes
+constexpr int kFp4Codes = kRow / 2;         // FP4 row: 288 bytes of e2m1 codes (two per byte) ...
+constexpr int kFp4Row = kFp4Codes + kRow / 16;   // ... then 36 e8m0 scales (one per 16 values): 324 bytes
 constexpr int kMaxSq = 4;
 constexpr int kMaxRows = 1 << 16;   // batch * Sq handled by the planner
 

@@ -134,6 +134,8 @@ template <> struct Cfg<1> {
   static constexpr int kEpWarps = 4;           // rank 0: four epilogue warps (512 columns each)
 };
 template <> struct Cfg<2> : Cfg<1> {};
+// FP4 cache (bf16 operands): the FP8 roles and layout, smaller raw copies
+template <> struct Cfg<4> : Cfg<1> {};
 // sparse decode over the bf16 cache: the bf16 plan, K and V gathered by rows
 template <> struct Cfg<3> : Cfg<0> {};
 constexpr int kGatherWarps = 3;          // sparse: warps 0, 2, 3 of each rank copy one half page of a tile each
@@ -334,6 +336,40 @@ __device__ __forceinline__ bool dequant_group(const uint8_t* row, int g, uint32_
   }
 }
 
+// FP4 row: value group g (32 values) -> 16 bf16x2 words.  Codes are two
+// e2m1 per byte, value 2k in the low nibble of byte k, so the group is the
+// 16 bytes at 16g (word-aligned: rows are 324 bytes); its two e8m0 scales
+// (values 32g..32g+15, then the next 16) are bytes kFp4Codes + 2g and + 1.
+// e2m1 -> f16 is exact in hardware (the low nibble becomes the low half),
+// the product with the power-of-two scale is exact in fp32, and with at most
+// two significant bits and a smallest bit of at least 2^-128 (> 2^-133, the
+// last bit of a bf16 subnormal) the bf16 value is the fp32 value's upper 16
+// bits.  Scale bytes up to 252 keep every product finite; 0xFF gives NaN.
+__device__ __forceinline__ float e8m0_f32(uint32_t e) {
+  return __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : (e << 23)));
+}
+
+__device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uint32_t* o) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 16 * g);
+  const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + kFp4Codes + 2 * g);
+  const float s0 = e8m0_f32(sc & 0xFFu), s1 = e8m0_f32(sc >> 8);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = w[i];
+    const float s = i < 2 ? s0 : s1;
+    uint32_t h[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(c));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
+      o[4 * i + k] = __byte_perm(__float_as_uint(f.x * s), __float_as_uint(f.y * s), 0x7632);
+    }
+  }
+}
+
 // Store 16 bf16x2 words (32 values of value group g) as token r of a
 // half-page slot whose 8-row atoms are `group_stride` bytes apart per row
 // group (chunk c = g/2 at c KiB inside the group, 128-byte rows, 128B
@@ -423,7 +459,12 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   constexpr int kSG = C::kSmGroups;             // softmax warp groups
   constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
-  constexpr bool kFp8 = kMode == 1 || kMode == 2;  // FP8 cache (raw rings, dequant warps)
+  constexpr bool kQuant = kMode == 1 || kMode == 2 || kMode == 4;  // FP8 or FP4 cache (raw rings, dequant warps)
+  constexpr bool kFp4 = kMode == 4;
+  // a quantised row and the half page the producer copies (its ring slots
+  // are sized for the larger FP8 half page)
+  constexpr uint32_t kQRow = kFp4 ? kFp4Row : kFp8Row;
+  constexpr uint32_t kQRaw = kHalf * kQRow;
   constexpr bool kF16 = kMode == 2;               // FP8 with f16 operands
   constexpr uint32_t kIdescS =                    // A = Q (TMEM), B = K (K-major)
       kF16 ? ptx::idesc_f16(128, kN, 0, 0) : ptx::idesc_bf16(128, kN, 0, 0);
@@ -462,14 +503,14 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     // sparse: each gather thread arrives once per tile (cp.async noinc)
     constexpr uint32_t kGatherThreads = 32u * kGatherWarps;
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(BAR(KFULL + s), kFp8 ? dq : (kMode == 3 ? kGatherThreads : 1u));
+      ptx::mbar_init(BAR(KFULL + s), kQuant ? dq : (kMode == 3 ? kGatherThreads : 1u));
       ptx::mbar_init(BAR(KEMPTY + s), 1);
       ptx::mbar_init(BAR(KFULLB + s), kMode == 3 ? kGatherThreads : 1u);
       ptx::mbar_init(BAR(KEMPTYB + s), 1);
     }
     // V slots: the TMA bytes (bf16) or the dequant warps (FP8)
     for (int s = 0; s < kMaxVSlots; ++s) {
-      ptx::mbar_init(BAR(VFULL + s), kFp8 ? dq : (kMode == 3 ? 32u : 1u));   // sparse: one warp per half page
+      ptx::mbar_init(BAR(VFULL + s), kQuant ? dq : (kMode == 3 ? 32u : 1u));   // sparse: one warp per half page
       ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
@@ -483,7 +524,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     for (int s = 0; s < kMailSlots; ++s) { ptx::mbar_init(BAR(MBFULL + s), 128); ptx::mbar_init(BAR(MBEMPTY + s), kEp); }
     for (int s = 0; s < kMaxRaw; ++s) {
       ptx::mbar_init(BAR(RAWFULL + s), 1);
-      ptx::mbar_init(BAR(RAWEMPTY + s), kFp8 ? dq : 1u);
+      ptx::mbar_init(BAR(RAWEMPTY + s), kQuant ? dq : 1u);
     }
     ptx::fence_barrier_init();
   }
@@ -689,9 +730,9 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               if (page < 0) {
                 ptx::mbar_arrive(BAR(RAWFULL + rs));
               } else {
-                ptx::mbar_arrive_expect_tx(BAR(RAWFULL + rs), kRawBytes);
-                const uint8_t* src = p.kv_fp8 + static_cast<size_t>(page) * (kPage * kFp8Row) + (hp & 1) * kRawBytes;
-                ptx::bulk_load(sbase + raw_off + static_cast<uint32_t>(rs) * kRawBytes, src, kRawBytes,
+                ptx::mbar_arrive_expect_tx(BAR(RAWFULL + rs), kQRaw);
+                const uint8_t* src = p.kv_quant + static_cast<size_t>(page) * (kPage * kQRow) + (hp & 1) * kQRaw;
+                ptx::bulk_load(sbase + raw_off + static_cast<uint32_t>(rs) * kRawBytes, src, kQRaw,
                                BAR(RAWFULL + rs), pol);
               }
               if (++rs == n_raw) { rs = 0; rphase ^= 1u; }
@@ -715,7 +756,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
       }
     }
-  } else if (kFp8 && active && (warp >= 8 || (warp == 2 && rank == 1))) {
+  } else if (kQuant && active && (warp >= 8 || (warp == 2 && rank == 1))) {
     // ------------------------------------------------------------ FP8 dequant
     // raw half page -> rank 1: K slot (all 18 value groups, nine-chunk
     // layout); rank 0: V slot (the 16 latent groups).  Warp wq takes value
@@ -745,9 +786,15 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           if (!wait_warp<false>(BAR(RAWFULL + rs), rphase, hdr)) { ok = false; break; }
           uint32_t o0[16], o1[16];
           if (raw_flag[rs] == 0) {
-            const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + t * kFp8Row;
-            const bool r0 = dequant_group<kF16>(row, g, o0);
-            const bool r1 = dequant_group<kF16>(row + 16 * kFp8Row, g, o1);
+            const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + t * kQRow;
+            bool r0 = true, r1 = true;
+            if constexpr (kFp4) {
+              dequant_group_fp4(row, g, o0);
+              dequant_group_fp4(row + 16 * kQRow, g, o1);
+            } else {
+              r0 = dequant_group<kF16>(row, g, o0);
+              r1 = dequant_group<kF16>(row + 16 * kQRow, g, o1);
+            }
             if (kF16 && !range_flagged && __any_sync(0xffffffffu, !(r0 && r1))) {
               if (lane == 0) atomicExch(&hdr->fp8_range, 1);
               range_flagged = true;
@@ -1253,9 +1300,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   }
 }
 
-// Host-side launcher.  kMode 0: bf16 cache through the two 4-D tensor maps
-// (half-page boxes: nine chunks for rank 1, eight for rank 0); 1: FP8 cache
-// (p.kv_fp8; tensor maps unused).
+// Host-side launcher.  kMode 0: bf16 cache through the 4-D tensor maps
+// (half-page boxes: chunks 0..4 and 5..8 for rank 1, eight for rank 0);
+// 1 and 2: FP8 cache, 4: FP4 cache (p.kv_quant; tensor maps unused);
+// 3: sparse gather from the bf16 cache.
 template <int kMode>
 cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
                                const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
@@ -1297,6 +1345,12 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cuda
   if (e != cudaSuccess) return e;
   q.fp8_fallback = 1;
   return launch_decode_mode<1>(unused, unused, unused, q, n_pairs, pdl, stream);
+}
+
+cudaError_t launch_decode_fp4(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  return launch_decode_mode<4>(unused, unused, unused, p, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {

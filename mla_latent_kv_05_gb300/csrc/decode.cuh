@@ -11,7 +11,7 @@ namespace mla {
 struct DecodeParams {
   const __nv_bfloat16* q_abs;    // [B, Sq, 128, 512]
   const __nv_bfloat16* q_rope;   // [B, Sq, 128, 64]
-  const uint8_t* kv_fp8;         // fp8 cache [P, 64, 594] (fp8 mode)
+  const uint8_t* kv_quant;       // FP8 cache [P, 64, 594] or FP4 cache [P, 64, 324] (modes 1, 2, 4)
   const uint8_t* kv_bf16;        // bf16 cache [P, 64, 576] (read by address in the sparse mode)
   const int32_t* block_table;    // [B, max_pages]
   int batch, sq, num_pages, max_pages;
@@ -37,6 +37,7 @@ cudaError_t launch_sparse_prep(const int32_t* token_slots, int rows, int topk, i
 cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
                                const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
+cudaError_t launch_decode_fp4(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 // Sparse decode over the bf16 cache (p.kv_bf16, p.sp_slots; rows planned
 // with one query each).
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);

@@ -4,7 +4,8 @@ This module is the one piece shared by the float64 oracle tests and the CUDA
 path: it only draws random numbers and builds page tables. It holds none of the
 attention arithmetic. The FP8 cache is produced by rounding N(0,1) draws to
 e4m3 with torch's own cast and drawing the e8m0 scale bytes independently; the
-decoding of those bytes is done separately by each side.
+FP4 cache is uniform random bytes (two e2m1 codes each) and uniform scale
+bytes.  The decoding of those bytes is done separately by each side.
 
 Shapes follow the model records on the pages (DeepSeek-R1 / V3.2 records:
 kv_lora_rank 512; architecture guide section 1.1: 512 latent + 64 decoupled
@@ -26,7 +27,15 @@ PAGE_SIZE = 64
 FP8_SCALE_GROUP = 32
 FP8_NUM_SCALES = ROW_ELEMS // FP8_SCALE_GROUP   # 18
 FP8_ROW_BYTES = ROW_ELEMS + FP8_NUM_SCALES      # 594
+FP4_SCALE_GROUP = 16
+FP4_NUM_SCALES = ROW_ELEMS // FP4_SCALE_GROUP   # 36
+FP4_ROW_BYTES = ROW_ELEMS // 2 + FP4_NUM_SCALES # 324
 DEFAULT_SCALE = 1.0 / math.sqrt(128 + 64)       # 1/sqrt(d_h + d_h^R)
+
+
+def row_bytes_of(kv_dtype: str) -> int:
+    """Bytes of one cached token row in each cache format."""
+    return {"bf16": ROW_ELEMS * 2, "fp8": FP8_ROW_BYTES, "fp4": FP4_ROW_BYTES}[kv_dtype]
 
 
 @dataclass
@@ -34,11 +43,11 @@ class DecodeInputs:
     """One decode call's inputs, on the host (CPU tensors)."""
     q_absorbed: torch.Tensor   # [B, Sq, H, 512] bf16
     q_rope: torch.Tensor       # [B, Sq, H, 64] bf16
-    kv_cache: torch.Tensor     # bf16 [P, 64, 576] or uint8 [P, 64, 594]
+    kv_cache: torch.Tensor     # bf16 [P, 64, 576], uint8 [P, 64, 594] (fp8) or [P, 64, 324] (fp4)
     block_table: torch.Tensor  # int32 [B, max_pages], -1 where unused
     seq_lens: torch.Tensor     # int32 [B]
     scale: float
-    kv_dtype: str              # "bf16" or "fp8"
+    kv_dtype: str              # "bf16", "fp8" or "fp4"
     name: str = ""
     meta: dict = field(default_factory=dict)
 
@@ -59,7 +68,7 @@ class DecodeInputs:
         return int(self.block_table.shape[1])
 
 
-# The five workloads: name -> parameters.  seq is either an int (uniform) or
+# The dense workloads: name -> parameters.  seq is either an int (uniform) or
 # ("uniform", lo, hi) for lengths drawn from the seed.
 WORKLOADS = {
     1: dict(name="oracle-sized B1 seq256 bf16", batch=1, sq=1, seq=256,
@@ -72,6 +81,8 @@ WORKLOADS = {
             kv_dtype="fp8"),
     5: dict(name="B4 Sq2 causal seq131072 bf16", batch=4, sq=2, seq=131072,
             kv_dtype="bf16"),
+    7: dict(name="fp4 B128 seq8192", batch=128, sq=1, seq=8192,
+            kv_dtype="fp4"),
 }
 
 
@@ -107,6 +118,23 @@ def _fp8_cache(gen: torch.Generator, num_pages: int, page_size: int) -> torch.Te
     return out
 
 
+def _fp4_cache(gen: torch.Generator, num_pages: int, page_size: int,
+               scale_lo: int = 120, scale_hi: int = 130) -> torch.Tensor:
+    """[P, page, 324] uint8: 288 uniform random bytes (576 e2m1 codes, two per
+    byte) followed by 36 e8m0 exponent bytes drawn uniformly from
+    [scale_lo, scale_hi]."""
+    out = torch.empty((num_pages, page_size, FP4_ROW_BYTES), dtype=torch.uint8)
+    step = 1024
+    nc = ROW_ELEMS // 2
+    for p0 in range(0, num_pages, step):
+        p1 = min(num_pages, p0 + step)
+        out[p0:p1, :, :nc] = torch.randint(0, 256, (p1 - p0, page_size, nc), generator=gen,
+                                           dtype=torch.int64).to(torch.uint8)
+        out[p0:p1, :, nc:] = torch.randint(scale_lo, scale_hi + 1, (p1 - p0, page_size, FP4_NUM_SCALES),
+                                           generator=gen, dtype=torch.int64).to(torch.uint8)
+    return out
+
+
 def make_inputs(batch: int, sq: int, seq_lens, kv_dtype: str = "bf16",
                 seed: int = 0, physical_pages: int | None = None,
                 max_pages: int | None = None, scale: float = DEFAULT_SCALE,
@@ -139,6 +167,8 @@ def make_inputs(batch: int, sq: int, seq_lens, kv_dtype: str = "bf16",
         cache = _randn_bf16(gen, (n_phys, page_size, ROW_ELEMS))
     elif kv_dtype == "fp8":
         cache = _fp8_cache(gen, n_phys, page_size)
+    elif kv_dtype == "fp4":
+        cache = _fp4_cache(gen, n_phys, page_size)
     else:
         raise ValueError(kv_dtype)
     return DecodeInputs(q_absorbed=q_abs, q_rope=q_rope, kv_cache=cache,
@@ -157,7 +187,7 @@ def workload_seq_lens(workload: int) -> list[int]:
 
 
 def make_workload(workload: int) -> DecodeInputs:
-    """The seeded inputs of one of the five workloads (seed = 1000 + index)."""
+    """The seeded inputs of one of the dense workloads (seed = 1000 + index)."""
     w = WORKLOADS[workload]
     return make_inputs(w["batch"], w["sq"], workload_seq_lens(workload),
                        kv_dtype=w["kv_dtype"], seed=seed_for(workload),
@@ -173,7 +203,7 @@ def workload_counts(inp: DecodeInputs) -> dict:
     seq = [int(s) for s in inp.seq_lens.tolist()]
     sq = inp.sq
     H = int(inp.q_absorbed.shape[2])
-    row_bytes = ROW_ELEMS * 2 if inp.kv_dtype == "bf16" else FP8_ROW_BYTES
+    row_bytes = row_bytes_of(inp.kv_dtype)
     kv_tokens = sum(max(s, 0) for s in seq)
     pairs = 0
     for s in seq:
@@ -257,7 +287,7 @@ def sparse_counts(inp: SparseInputs) -> dict:
     lists) and FLOPs."""
     d = inp.dense
     H = int(d.q_absorbed.shape[2])
-    row_bytes = ROW_ELEMS * 2 if d.kv_dtype == "bf16" else FP8_ROW_BYTES
+    row_bytes = row_bytes_of(d.kv_dtype)
     pairs = int((inp.token_slots >= 0).sum())
     rows = inp.batch * inp.sq
     bytes_ = (pairs * row_bytes + rows * H * (D_LATENT + D_ROPE) * 2 + rows * H * D_LATENT * 2 + rows * H * 4

@@ -12,11 +12,13 @@ Sources (web pages, cited by title and section):
     98.24 % reduction, 9.21 GB at 128K), section 4 (e4m3 max normal 448).
   * "DeepSeek-R1" model record: 61 x 576 x 2 = 70,272 B/token; engine kernel
     constraints (1) page-block size 64 and (2) e4m3 latents with one e8m0
-    scale per 32 values inlined in each token row.
+    scale per 32 values inlined in each token row, and an FP4 variant of
+    288 B per 512-value row.
   * "DeepSeek-V3.2" model record: the same cache figures.
 
 Modules:
   fp8_codec     e4m3 (OCP E4M3FN) and e8m0 decoders, FP8 row dequantisation
+  fp4_codec     e2m1 (OCP MX FP4) decoder, FP4 row dequantisation
   mla_oracle    absorbed and un-absorbed attention, paged gather, LSE merge
   closed_forms  the pages' cache-size arithmetic
 
@@ -25,4 +27,4 @@ itself (closed forms printed on the pages, torch's float8 casts, torch's
 scaled-dot-product attention in float64, the absorption identity, brute-force
 special cases and invariants).  No function is "parity unpinned".
 """
-from . import closed_forms, fp8_codec, mla_oracle  # noqa: F401
+from . import closed_forms, fp4_codec, fp8_codec, mla_oracle  # noqa: F401

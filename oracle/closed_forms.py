@@ -57,3 +57,13 @@ def fp8_row_bytes(values: int = D_LATENT + D_ROPE, group: int = 32) -> int:
 
 def fp8_page_bytes(page_size: int = PAGE_SIZE) -> int:
     return page_size * fp8_row_bytes()
+
+
+def fp4_row_bytes(values: int = D_LATENT + D_ROPE, group: int = 16) -> int:
+    """e2m1 codes, two per byte, plus one e8m0 byte per `group` values (the
+    reading taken for the FP4 row): 288 for the record's 512-value row."""
+    return values // 2 + values // group
+
+
+def fp4_page_bytes(page_size: int = PAGE_SIZE) -> int:
+    return page_size * fp4_row_bytes()

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = declared_functions()
-    for n in ("mla_decode_bf16", "mla_decode_fp8", "mla_combine_splits", "mla_workspace_size",
+    for n in ("mla_decode_bf16", "mla_decode_fp8", "mla_decode_fp4", "mla_combine_splits", "mla_workspace_size",
               "mla_get_status", "mla_status_string", "mla_decode_sparse_bf16", "mla_workspace_size_sparse"):
         assert n in names
 
@@ -58,6 +58,12 @@ def test_host_validation_without_gpu(lib):
     assert rc == -2
     rc = lib.mla_decode_fp8(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(float("nan")),
                             fake, fake, fake, 1 << 30, z)
+    assert rc == -1
+    rc = lib.mla_decode_fp4(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(float("inf")),
+                            fake, fake, fake, 1 << 30, z)
+    assert rc == -1
+    rc = lib.mla_decode_fp4(fake, fake, ctypes.c_void_p(0x1004), fake, fake, 1, 1, 128, 8, 64, 4,
+                            ctypes.c_float(0.1), fake, fake, fake, 1 << 30, z)   # cache not 16-byte aligned
     assert rc == -1
     for bad_scale in (0.0, -0.1):
         rc = lib.mla_decode_bf16(fake, fake, fake, fake, fake, 1, 1, 128, 8, 64, 4, ctypes.c_float(bad_scale),

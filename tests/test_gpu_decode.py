@@ -13,7 +13,7 @@ import torch
 
 from mla_latent_kv_05_gb300 import binding
 from mla_latent_kv_05_gb300 import inputs as gen
-from oracle import mla_oracle
+from oracle import fp4_codec, mla_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def to_dev(inp, dev="cuda"):
 def run_gpu(inp, d=None):
     d = d or to_dev(inp)
     ws = binding.alloc_workspace(inp.batch, inp.sq)
-    fn = binding.mla_decode_bf16 if inp.kv_dtype == "bf16" else binding.mla_decode_fp8
+    fn = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8, "fp4": binding.mla_decode_fp4}[inp.kv_dtype]
     out, lse = fn(d["q"], d["qr"], d["kv"], d["bt"], d["sl"], inp.scale, workspace=ws)
     st = binding.mla_get_status(ws)
     return out, lse, st
@@ -285,6 +285,69 @@ def test_fp8_query_beyond_f16_range_takes_the_exact_pass(cuda_device):
 
 def test_fp8_bad_page_sets_status(cuda_device):
     inp = gen.make_inputs(2, 1, [100, 64], kv_dtype="fp8", seed=4)
+    inp.block_table[1, 0] = -3
+    _, _, st = run_gpu(inp)
+    assert st == -5
+
+
+def _dequant4_bf16(raw):
+    return torch.from_numpy(fp4_codec.dequant_rows(raw.numpy())).to(torch.bfloat16)
+
+
+# FP4 rows: 288 code bytes (two e2m1 per byte, value 2k in the low nibble),
+# then 36 e8m0 scales, one per 16 values.
+
+def test_fp4_every_token_position_is_bit_exact_dequant(cuda_device):
+    # As for FP8: batch row b attends to token b of its page alone (only the
+    # first RoPE dimension of the query is set; token b's first RoPE value is
+    # +6 * 2^4 against -6 * 2^4 for every other token, so every other weight
+    # is exp(-16 * 192 / sqrt(192)) ~ 1e-96 = 0 in fp32), and out = token b's
+    # dequantised latent row exactly.  Token b's first code bytes cover all
+    # sixteen e2m1 codes in both nibbles, and its scales span a wide range
+    # (kept where every value is a normal bf16 number, so the MMA's copy is
+    # exact).
+    n = 64
+    inp = gen.make_inputs(n, 1, [n] * n, kv_dtype="fp4", seed=35)
+    inp.q_absorbed.zero_()
+    inp.q_rope.zero_()
+    inp.q_rope[..., 0] = 16.0
+    scales = [2, 10, 100, 119, 127, 128, 135, 150, 200, 252]
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        rows = inp.kv_cache[page]
+        rows[:, 256:288] = 0                     # RoPE codes (values 512..575): zero ...
+        rows[:, 288 + 32] = 131                  # ... scale 2^4 on values 512..527
+        rows[:, 256] = 0x0F                      # value 512 = -6 * 2^4 for every token ...
+        rows[b, 256] = 0x07                      # ... and +6 * 2^4 for token b
+        rows[b, :16] = torch.tensor([0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE,
+                                     0x01, 0x23, 0x45, 0x67, 0x89, 0xAB, 0xCD, 0xEF], dtype=torch.uint8)
+        rows[b, 288:288 + 32] = torch.tensor([scales[(b + k) % len(scales)] for k in range(32)], dtype=torch.uint8)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        want = _dequant4_bf16(inp.kv_cache[page, b])[:512]
+        got = out[b, 0].cpu()
+        assert torch.equal(got, want.expand(128, 512)), b   # value-exact (-0 == +0)
+
+
+@pytest.mark.parametrize("lens", [[1, 63, 64, 65, 200], [3000, 17]])
+def test_fp4_ragged(cuda_device, lens):
+    inp = gen.make_inputs(len(lens), 1, lens, kv_dtype="fp4", seed=17 + len(lens))
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_fp4_causal_split_rows(cuda_device):
+    inp = gen.make_inputs(3, 2, [70, 5000, 130], kv_dtype="fp4", seed=18)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_fp4_bad_page_sets_status(cuda_device):
+    inp = gen.make_inputs(2, 1, [100, 64], kv_dtype="fp4", seed=5)
     inp.block_table[1, 0] = -3
     _, _, st = run_gpu(inp)
     assert st == -5

@@ -1,4 +1,4 @@
-"""The five workloads at full size, in the launch configuration the benchmark
+"""The dense workloads at full size, in the launch configuration the benchmark
 times, checked against the float64 oracle on sampled query rows (all 128
 heads and 512 columns of each sampled row), plus properties that hold at any
 size (finite outputs, lse bounds)."""
@@ -21,7 +21,7 @@ def sampled_rows(inp, k=4):
     return [(b, i) for b in sorted(bs) for i in range(inp.sq)]
 
 
-@pytest.mark.parametrize("workload", [2, 3, 4, 5])
+@pytest.mark.parametrize("workload", [2, 3, 4, 5, 7])
 def test_workload_full_size(cuda_device, workload):
     inp = gen.make_workload(workload)
     out, lse, st = run_gpu(inp)

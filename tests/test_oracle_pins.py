@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from oracle import closed_forms as cf
-from oracle import fp8_codec, mla_oracle
+from oracle import fp4_codec, fp8_codec, mla_oracle
 from mla_latent_kv_05_gb300 import inputs as gen
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_forms.txt")
@@ -44,6 +44,7 @@ def test_closed_forms_match_printed_values():
         "e4m3_max_normal": float(np.nanmax(fp8_codec.e4m3fn_to_float64(np.arange(256, dtype=np.uint8)))),
         "fp8_scales_per_row_group": fp8_codec.SCALE_GROUP,
         "page_block_size": cf.PAGE_SIZE,
+        "fp4_row_bytes_512_values": cf.fp4_row_bytes(512),
     }
     assert set(computed) == set(g)
     for k, (v, tol) in g.items():
@@ -52,6 +53,7 @@ def test_closed_forms_match_printed_values():
     assert cf.mla_cache_bytes() == 9_210_691_584
     assert cf.mha_cache_bytes() == 523_986_010_112
     assert cf.fp8_row_bytes() == 594 and cf.fp8_page_bytes() == 38_016
+    assert cf.fp4_row_bytes() == fp4_codec.ROW_BYTES == 324 and cf.fp4_page_bytes() == 20_736
 
 
 def test_e4m3_table_matches_torch_cast():
@@ -90,6 +92,55 @@ def test_fp8_row_dequant_layout_against_torch():
     assert np.array_equal(as_bf16, mine)
 
 
+def test_e2m1_table_is_the_ocp_value_set():
+    # OCP MX FP4 E2M1: the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 in
+    # code order, the sign bit negating them; no NaN or infinity
+    v = fp4_codec.e2m1_to_float64(np.arange(16))
+    assert list(v[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(v[8:], -v[:8])
+    assert np.signbit(v[8]) and not np.signbit(v[0])
+    assert np.all(np.isfinite(v))
+
+
+def test_fp4_row_layout_by_hand():
+    row = np.zeros(324, dtype=np.uint8)
+    row[0] = 0x21          # value 0: code 1 (0.5), value 1: code 2 (1.0)
+    row[7] = 0xF7          # value 14: code 7 (6), value 15: code 15 (-6)
+    row[8] = 0x3B          # value 16: code 11 (-1.5), value 17: code 3 (1.5)
+    row[287] = 0x5C        # value 574: code 12 (-2), value 575: code 5 (3)
+    row[288] = 127         # scale of values 0..15: 1
+    row[289] = 130         # values 16..31: 8
+    row[323] = 125         # values 560..575: 1/4
+    v = fp4_codec.dequant_rows(row)
+    assert v.shape == (576,)
+    assert (v[0], v[1], v[14], v[15]) == (0.5, 1.0, 6.0, -6.0)
+    assert (v[16], v[17]) == (-12.0, 12.0)
+    assert (v[574], v[575]) == (-0.5, 0.75)
+    assert np.count_nonzero(v) == 8
+
+
+def test_fp4_value_k_takes_scale_k_div_16():
+    # every code 2 (= 1.0), so each value is its scale: 2^(byte - 127)
+    inp = gen.make_inputs(1, 1, [64], kv_dtype="fp4", seed=9)
+    raw = inp.kv_cache.numpy().copy()
+    raw[..., :288] = 0x22
+    v = fp4_codec.dequant_rows(raw)
+    sc = raw[..., 288:].astype(np.int64)
+    for k in (0, 15, 16, 31, 100, 511, 512, 575):
+        assert np.array_equal(v[..., k], np.exp2(sc[..., k // 16] - 127.0)), k
+
+
+def test_fp4_generated_rows_are_bf16_exact():
+    inp = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp4", seed=3)
+    assert inp.kv_cache.shape[-1] == 324
+    v = fp4_codec.dequant_rows(inp.kv_cache.numpy())
+    as_bf16 = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(as_bf16, v)
+    # both nibbles carry all sixteen codes somewhere
+    codes = fp4_codec.unpack_codes(inp.kv_cache.numpy()[..., :288])
+    assert set(np.unique(codes[..., 0::2])) == set(range(16)) == set(np.unique(codes[..., 1::2]))
+
+
 def _f64(t):
     return t.to(torch.float64).numpy()
 
@@ -110,7 +161,8 @@ def _gathered(inp, b, i=0):
     return mla_oracle.gather_rows(rows, inp.block_table[b].numpy(), n)
 
 
-@pytest.mark.parametrize("seq,kv", [([256], "bf16"), ([1, 63, 64, 65, 200], "bf16"), ([130, 7], "fp8")])
+@pytest.mark.parametrize("seq,kv", [([256], "bf16"), ([1, 63, 64, 65, 200], "bf16"), ([130, 7], "fp8"),
+                                    ([130, 7], "fp4")])
 def test_attend_matches_torch_sdpa(seq, kv):
     inp = gen.make_inputs(len(seq), 1, seq, kv_dtype=kv, seed=11)
     for b in range(len(seq)):
