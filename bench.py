@@ -333,9 +333,9 @@ def run_ours(args):
         bt = inp.block_table.to(dev)
         sl = inp.seq_lens.to(dev)
         ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
-        # planner, attention, merge (FP8: the exact pass after the f16 pass is
+        # planner, attention, merge (FP8, FP4: the exact pass after the f16 pass is
         # a fourth launch, which returns at once unless needed)
-        launches = 4 if inp.kv_dtype == "fp8" else 3
+        launches = 3 if inp.kv_dtype == "bf16" else 4
         uploads = [(inp.block_table.pin_memory(), bt), (inp.seq_lens.pin_memory(), sl)]
 
         def call(qb, qrb, extra, outb, lseb):

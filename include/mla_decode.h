@@ -147,8 +147,11 @@ int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope,
  *   v[k] = e2m1(nibble k) * 2^(byte[288 + k/16] - 127),
  * e2m1 = OCP MX FP4: sign, 2 exponent bits (bias 1), 1 mantissa bit.
  * The values are exact in bf16 for scale bytes in [0, 252] (255 is NaN;
- * 253 and 254 overflow) and are attended with bf16 operands, as the bf16
- * path does.  kv_cache must be 16-byte aligned.  Arguments, layouts,
+ * 253 and 254 overflow).  As for FP8, when every scale byte of the call
+ * lies in [113, 140] and every query value fits f16 the values are exact in
+ * f16 too and the MMAs take f16 operands; otherwise a second pass
+ * recomputes the call with bf16 operands.  kv_cache must be 16-byte
+ * aligned.  Arguments, layouts,
  * results and errors are otherwise those of mla_decode_bf16. */
 int mla_decode_fp4(const uint16_t* q_absorbed, const uint16_t* q_rope,
                    const uint8_t* kv_cache, const int32_t* block_table,

@@ -30,7 +30,7 @@ struct PlanHeader {
   int n_comb;            // rows the merge kernel must write
   int pairs_per_group;   // pairs that serve one query index
   int abort_flag;        // set by the first wait that times out; all waits then give up
-  int fp8_range;         // FP8 f16 pass: an input lies outside the f16-exact range (the exact pass recomputes)
+  int fp8_range;         // FP8/FP4 f16 pass: an input lies outside the f16-exact range (the exact pass recomputes)
   int pad[8];
 };
 

@@ -134,8 +134,10 @@ template <> struct Cfg<1> {
   static constexpr int kEpWarps = 4;           // rank 0: four epilogue warps (512 columns each)
 };
 template <> struct Cfg<2> : Cfg<1> {};
-// FP4 cache (bf16 operands): the FP8 roles and layout, smaller raw copies
+// FP4 cache: the FP8 roles and layout, smaller raw copies; 4 = bf16
+// operands (exact), 5 = f16 operands
 template <> struct Cfg<4> : Cfg<1> {};
+template <> struct Cfg<5> : Cfg<1> {};
 // sparse decode over the bf16 cache: the bf16 plan, K and V gathered by rows
 template <> struct Cfg<3> : Cfg<0> {};
 constexpr int kGatherWarps = 3;          // sparse: warps 0, 2, 3 of each rank copy one half page of a tile each
@@ -173,13 +175,14 @@ constexpr uint32_t kTmemCols = 512;
 
 // P.V: A = P (K-major), B = V (MN-major); bf16, or f16 in the FP8 f16 mode
 template <int kMode>
-constexpr uint32_t kIdescPV = kMode == 2 ? ptx::idesc_f16(128, 256, 0, 1) : ptx::idesc_bf16(128, 256, 0, 1);
+constexpr uint32_t kIdescPV =
+    (kMode == 2 || kMode == 5) ? ptx::idesc_f16(128, 256, 0, 1) : ptx::idesc_bf16(128, 256, 0, 1);
 
 constexpr float kLn2 = 0.69314718055994530942f;
 // log2 units: P <= 2^16 (exact in relative terms; O stays far from fp32
 // overflow).  The FP8 f16 mode keeps P <= 2^15, inside the f16 range.
 template <int kMode>
-constexpr float kRescaleThreshold = kMode == 2 ? 15.0f : 16.0f;
+constexpr float kRescaleThreshold = (kMode == 2 || kMode == 5) ? 15.0f : 16.0f;
 
 // FP8 f16 mode: a scale exponent e in [113, 134] makes every e4m3 code times
 // 2^(e-127) an exact f16 number (largest 448 * 2^7 = 57344 < 65504; smallest
@@ -370,6 +373,36 @@ __device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uin
   }
 }
 
+// FP4 f16 mode: the same group as 16 f16x2 words, each the exact hardware
+// e2m1 -> f16 conversion times the f16 scale 2^(e-127) (a packed f16
+// multiply).  Exact for both scale bytes in [kFp4F16ScaleLo, kFp4F16ScaleHi]:
+// the largest product 6 * 2^13 = 49152 fits f16, every product is a
+// multiple of 2^-15, above the f16 subnormal step, and the scale itself is a
+// normal f16 number.  Returns false for a scale outside that range.
+constexpr uint32_t kFp4F16ScaleLo = 113, kFp4F16ScaleHi = 140;
+
+__device__ __forceinline__ bool dequant_group_fp4_f16(const uint8_t* row, int g, uint32_t* o) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 16 * g);
+  const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + kFp4Codes + 2 * g);
+  const uint32_t e0 = sc & 0xFFu, e1 = sc >> 8;
+  const bool in_range = e0 >= kFp4F16ScaleLo && e0 <= kFp4F16ScaleHi && e1 >= kFp4F16ScaleLo && e1 <= kFp4F16ScaleHi;
+  const uint32_t f0 = ((e0 - 112u) & 31u) << 10, f1 = ((e1 - 112u) & 31u) << 10;
+  const uint32_t s0 = f0 | (f0 << 16), s1 = f1 | (f1 << 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = w[i];
+    const uint32_t s = i < 2 ? s0 : s1;
+    uint32_t h[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(c));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * i + k]) : "r"(h[k]), "r"(s));
+  }
+  return in_range;
+}
+
 // Store 16 bf16x2 words (32 values of value group g) as token r of a
 // half-page slot whose 8-row atoms are `group_stride` bytes apart per row
 // group (chunk c = g/2 at c KiB inside the group, 128-byte rows, 128B
@@ -459,13 +492,13 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   constexpr int kSG = C::kSmGroups;             // softmax warp groups
   constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
-  constexpr bool kQuant = kMode == 1 || kMode == 2 || kMode == 4;  // FP8 or FP4 cache (raw rings, dequant warps)
-  constexpr bool kFp4 = kMode == 4;
+  constexpr bool kQuant = kMode == 1 || kMode == 2 || kMode == 4 || kMode == 5;  // FP8 or FP4 cache (raw rings, dequant warps)
+  constexpr bool kFp4 = kMode == 4 || kMode == 5;
   // a quantised row and the half page the producer copies (its ring slots
   // are sized for the larger FP8 half page)
   constexpr uint32_t kQRow = kFp4 ? kFp4Row : kFp8Row;
   constexpr uint32_t kQRaw = kHalf * kQRow;
-  constexpr bool kF16 = kMode == 2;               // FP8 with f16 operands
+  constexpr bool kF16 = kMode == 2 || kMode == 5;  // FP8 or FP4 with f16 operands
   constexpr uint32_t kIdescS =                    // A = Q (TMEM), B = K (K-major)
       kF16 ? ptx::idesc_f16(128, kN, 0, 0) : ptx::idesc_bf16(128, kN, 0, 0);
   constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
@@ -788,7 +821,10 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           if (raw_flag[rs] == 0) {
             const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + t * kQRow;
             bool r0 = true, r1 = true;
-            if constexpr (kFp4) {
+            if constexpr (kFp4 && kF16) {
+              r0 = dequant_group_fp4_f16(row, g, o0);
+              r1 = dequant_group_fp4_f16(row + 16 * kQRow, g, o1);
+            } else if constexpr (kFp4) {
               dequant_group_fp4(row, g, o0);
               dequant_group_fp4(row + 16 * kQRow, g, o1);
             } else {
@@ -1302,7 +1338,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
 
 // Host-side launcher.  kMode 0: bf16 cache through the 4-D tensor maps
 // (half-page boxes: chunks 0..4 and 5..8 for rank 1, eight for rank 0);
-// 1 and 2: FP8 cache, 4: FP4 cache (p.kv_quant; tensor maps unused);
+// 1 and 2: FP8 cache, 4 and 5: FP4 cache (p.kv_quant; tensor maps unused;
+// 2 and 5 take f16 operands, 1 and 4 bf16);
 // 3: sparse gather from the bf16 cache.
 template <int kMode>
 cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
@@ -1350,7 +1387,14 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cuda
 cudaError_t launch_decode_fp4(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return launch_decode_mode<4>(unused, unused, unused, p, n_pairs, pdl, stream);
+  // as for FP8: the f16-operand pass, then the exact bf16-operand pass,
+  // which returns at once unless the first pass flagged an input
+  DecodeParams q = p;
+  q.fp8_fallback = 0;
+  cudaError_t e = launch_decode_mode<5>(unused, unused, unused, q, n_pairs, pdl, stream);
+  if (e != cudaSuccess) return e;
+  q.fp8_fallback = 1;
+  return launch_decode_mode<4>(unused, unused, unused, q, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {

@@ -16,7 +16,7 @@ struct DecodeParams {
   const int32_t* block_table;    // [B, max_pages]
   int batch, sq, num_pages, max_pages;
   float scale_log2;              // softmax scale * log2(e)
-  int fp8_fallback;              // FP8 exact pass: run only if the f16 pass flagged its inputs
+  int fp8_fallback;              // FP8/FP4 exact pass: run only if the f16 pass flagged its inputs
   const int32_t* sp_slots;       // sparse decode: compacted slot lists [rows, topk] (workspace)
   int topk;
   __nv_bfloat16* out;            // [B, Sq, 128, 512]

@@ -346,6 +346,24 @@ def test_fp4_causal_split_rows(cuda_device):
     assert_close(out, lse, *oracle(inp))
 
 
+@pytest.mark.parametrize("scale_byte", [112, 140, 141])
+def test_fp4_scale_at_the_f16_range_edges(cuda_device, scale_byte):
+    # the f16-operand pass takes scale bytes in [113, 140]; 112 and 141 make
+    # the exact bf16-operand pass recompute the call, and all three must
+    # match the oracle.  The edge scale sits on latent values 48..63 of one
+    # token (up to 6 * 2^14 there), and the query is zero on those
+    # dimensions, so they reach the output but not the scores (scores in the
+    # thousands would put fp32 accumulation error above the lse bound).
+    inp = gen.make_inputs(2, 1, [150, 64], kv_dtype="fp4", seed=19)
+    page = int(inp.block_table[0, 1])
+    inp.kv_cache[page, 5, 288 + 3] = scale_byte
+    inp.q_absorbed[0, :, :, 48:64] = 0
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, lse, *oracle(inp))
+
+
 def test_fp4_bad_page_sets_status(cuda_device):
     inp = gen.make_inputs(2, 1, [100, 64], kv_dtype="fp4", seed=5)
     inp.block_table[1, 0] = -3
