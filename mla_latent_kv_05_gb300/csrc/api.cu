@@ -125,9 +125,10 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   g_prof_before = g_prof_after = nullptr;
   const bool pdl = ev0 == nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  const cudaError_t le = kind == CacheKind::kFp8   ? launch_decode_fp8(p, ppg * sq, pdl, stream)
-                         : kind == CacheKind::kFp4 ? launch_decode_fp4(p, ppg * sq, pdl, stream)
-                                                   : launch_decode_bf16(tmap_k, tmap_kb, tmap_v, p, ppg * sq, pdl, stream);
+  cudaError_t le;
+  if (kind == CacheKind::kFp8) le = launch_decode_fp8(p, ppg * sq, pdl, stream);
+  else if (kind == CacheKind::kFp4) le = launch_decode_fp4(p, ppg * sq, pdl, stream);
+  else le = launch_decode_bf16(tmap_k, tmap_kb, tmap_v, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -276,8 +277,8 @@ int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope, const ui
                     const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
                     int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  return run_decode(CacheKind::kBf16, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
-                    page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+  return run_decode(CacheKind::kBf16, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads,
+                    num_pages, page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 int mla_decode_bf16_noalloc(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint16_t* kv_cache,
@@ -298,8 +299,8 @@ int mla_decode_bf16_noalloc(const uint16_t* q_absorbed, const uint16_t* q_rope, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the status word and the abort flag must start at zero for this call
   if (cudaMemsetAsync(scratch, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
-  st = run_decode(CacheKind::kBf16, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
-                  page_size, max_pages, softmax_scale, out, lse, scratch, kStaticScratchBytes, stream);
+  st = run_decode(CacheKind::kBf16, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads,
+                  num_pages, page_size, max_pages, softmax_scale, out, lse, scratch, kStaticScratchBytes, stream);
   if (st != MLA_OK) return st;
   if (device_status &&
       cudaMemcpyAsync(device_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
@@ -311,8 +312,8 @@ int mla_decode_fp8(const uint16_t* q_absorbed, const uint16_t* q_rope, const uin
                    const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
                    int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  return run_decode(CacheKind::kFp8, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads, num_pages,
-                    page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+  return run_decode(CacheKind::kFp8, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads,
+                    num_pages, page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 int mla_decode_fp4(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint8_t* kv_cache,
