@@ -1,4 +1,4 @@
-"""The seeded input generator: determinism and the structure of the five workloads."""
+"""The seeded input generator: determinism and the structure of the workloads."""
 import torch
 
 from mla_latent_kv_05_gb300 import inputs as gen
@@ -49,3 +49,24 @@ def test_counts_workload2():
     c = gen.workload_counts(gen.make_inputs(32, 1, [4096] * 32, seed=0, num_heads=128))
     assert c["kv_tokens"] == 32 * 4096
     assert c["flops"] == 32 * 4096 * 2 * 128 * (576 + 512)
+
+
+def test_fp4_cache_bytes_and_scales():
+    a = gen.make_inputs(2, 1, [100, 3], kv_dtype="fp4", seed=1)
+    b = gen.make_inputs(2, 1, [100, 3], kv_dtype="fp4", seed=1)
+    assert torch.equal(a.kv_cache, b.kv_cache)
+    assert a.kv_cache.shape == (3, 64, 324) and a.kv_cache.dtype == torch.uint8
+    sc = a.kv_cache[..., 288:]
+    assert int(sc.min()) >= 120 and int(sc.max()) <= 130
+    # both nibbles of the code bytes take all sixteen values
+    codes = a.kv_cache[..., :288]
+    assert set((codes & 0xF).unique().tolist()) == set(range(16)) == set((codes >> 4).unique().tolist())
+
+
+def test_counts_per_cache_format():
+    # the algorithmic KV bytes per token: 1152 (bf16), 594 (fp8), 324 (fp4)
+    for kv, row in (("bf16", 1152), ("fp8", 594), ("fp4", 324)):
+        c = gen.workload_counts(gen.make_inputs(2, 1, [100, 28], kv_dtype=kv, seed=0))
+        assert c["kv_bytes"] == 128 * row, kv
+    assert gen.WORKLOADS[7]["kv_dtype"] == "fp4"
+    assert gen.WORKLOADS[7]["batch"] == gen.WORKLOADS[4]["batch"] and gen.WORKLOADS[7]["seq"] == gen.WORKLOADS[4]["seq"]
