@@ -1,8 +1,8 @@
 """Benchmark: MLA decode over a paged latent KV cache on GB300.
 
 One step = one full decode call through the C ABI (split-KV planner, paired
-tcgen05 attention kernel, LSE merge) over one batch of synthetic inputs that
-are already resident in HBM.  Default workload: batch 64, Sq 1, seq_lens
+tcgen05 attention kernel that also merges its split rows) over one batch of
+synthetic inputs that are already resident in HBM.  Default workload: batch 64, Sq 1, seq_lens
 drawn uniformly in [1, 32768] (seed 1003), bf16 cache with shuffled pages.
 
 Printed (one JSON line): KV-tokens/s of the whole job, ms/step, the
@@ -152,10 +152,17 @@ class ClockSampler:
                 "samples": len(rows), "samples_under_load": len(loaded)}
 
 
-def dist_setup():
+def dist_setup(gpus: int | None = None):
+    """Rank, world size and local rank from the launcher's environment.
+    `--gpus N` must match the launcher's world size: N ranks are started by
+    torch.distributed.run (one process per GPU), never by this script, so a
+    mismatch is an error rather than a silent one-GPU run."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if gpus is not None and gpus != world:
+        raise SystemExit(f"bench.py: --gpus {gpus} but WORLD_SIZE={world}; launch N ranks with "
+                         f"python -m torch.distributed.run --nproc-per-node {gpus} bench.py --gpus {gpus} ...")
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
@@ -252,7 +259,7 @@ def load_problem(workload: int):
 
 
 def run_reference(args):
-    world, rank, local = dist_setup()
+    world, rank, local = dist_setup(args.gpus)
     if rank != 0:
         return 0
     inp, sp = load_problem(args.workload)
@@ -302,7 +309,7 @@ def workload_config(workload: int, inp, sp=None) -> dict:
 
 def run_ours(args):
     from mla_latent_kv_05_gb300 import binding
-    world, rank, local = dist_setup()
+    world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp, sp = load_problem(args.workload)
@@ -313,12 +320,13 @@ def run_ours(args):
     lse = torch.empty((inp.batch, inp.sq, 128), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     if sp is not None:
-        # sparse top-k decode: four launches per call (compaction, planner,
-        # attention, merge); the per-step inputs are q, q_rope and the lists
+        # sparse top-k decode: three launches per call (compaction, planner,
+        # attention with the split merge); the per-step inputs are q, q_rope
+        # and the lists
         counts = gen.sparse_counts(sp)
         slots = sp.token_slots.to(dev)
         ws = binding.alloc_workspace_sparse(inp.batch, inp.sq, sp.topk, dev)
-        launches = 4
+        launches = 3
         uploads = [(sp.token_slots.pin_memory(), slots)]
 
         def call(qb, qrb, extra, outb, lseb):
@@ -333,9 +341,10 @@ def run_ours(args):
         bt = inp.block_table.to(dev)
         sl = inp.seq_lens.to(dev)
         ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
-        # planner, attention, merge (FP8, FP4: the exact pass after the f16 pass is
-        # a fourth launch, which returns at once unless needed)
-        launches = 3 if inp.kv_dtype == "bf16" else 4
+        # planner, attention with the split merge (FP8, FP4: the exact pass
+        # after the f16 pass is a third launch, which returns at once unless
+        # needed)
+        launches = 2 if inp.kv_dtype == "bf16" else 3
         uploads = [(inp.block_table.pin_memory(), bt), (inp.seq_lens.pin_memory(), sl)]
 
         def call(qb, qrb, extra, outb, lseb):
@@ -506,6 +515,52 @@ def run_ours(args):
     return 0
 
 
+def run_wuv(args):
+    """Time the W^UV up-projection alone (mla_up_project_wuv) on `--wuv-rows`
+    row counts: CUDA events on its stream, median of --steps calls after
+    --warmup calls, an L2 flush (a 258 MB write) before each call.  One JSON
+    line per row count, against the measured HBM roofline: algorithmic bytes
+    = latent (rows x 128 x 512 bf16) + W^UV (128 x 128 x 512 bf16) + out
+    (rows x 128 x 128 bf16); FLOPs = 2 x rows x 128 x 128 x 512."""
+    from mla_latent_kv_05_gb300 import binding
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    g = torch.Generator().manual_seed(7)
+    w_uv = (torch.randn((128, 128, 512), generator=g) * 512 ** -0.5).to(torch.bfloat16).to(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for rows in [int(x) for x in args.wuv_rows.split(",")]:
+        lat = torch.randn((rows, 128, 512), generator=g).to(torch.bfloat16).to(dev)
+        out = torch.empty((rows, 128, 128), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            binding.mla_up_project_wuv(lat, w_uv, out=out, workspace=ws)
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            binding.mla_up_project_wuv(lat, w_uv, out=out, workspace=ws)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b) * 1e-3)
+        if binding.mla_get_status(ws) != 0:
+            raise RuntimeError("device status after the W^UV calls")
+        t = float(np.median(times))
+        nbytes = 2 * (rows * 128 * 512 + 128 * 128 * 512 + rows * 128 * 128)
+        flops = 2.0 * rows * 128 * 128 * 512
+        gbs = nbytes / t / 1e9
+        if rank == 0:
+            print(json.dumps({"metric": "W^UV up-projection us/call", "value": t * 1e6, "unit": "us",
+                              "higher_is_better": False, "rows": rows, "steps": args.steps,
+                              "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+                              "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                                           "frac": gbs / peaks["hbm"], "tflops": flops / t / 1e12}}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,11 +570,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--wuv-rows", default=None,
+                    help="time the W^UV up-projection alone on these row counts (e.g. 64,128,1024,4096)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.wuv_rows:
+        return run_wuv(args)
     return run_ours(args)
 
 

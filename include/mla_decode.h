@@ -72,12 +72,17 @@ typedef enum {
 
 /* Bytes of device workspace a decode call with these sizes needs on the
  * current device (the split-KV plan, per-split partial outputs and the
- * status word).  Returns MLA_OK and writes *bytes, or a negative status. */
+ * status word).  Returns MLA_OK and writes *bytes, or a negative status.
+ * The size does not depend on max_pages (the partials are bounded by the
+ * number of CTA pairs, not by the context length), so that argument is not
+ * taken; a status return keeps size and error apart. */
 int mla_workspace_size(int batch, int sq, int num_heads, int page_size, size_t* bytes);
 
 /* MLA decode over a bf16 latent cache (guide section 1.1; see top of file).
- * Queues: the split-KV planner, the paired tcgen05 decode kernel and the
- * LSE-merge kernel.  workspace: device memory of at least
+ * Queues two kernels: the split-KV planner, and the paired tcgen05 decode
+ * kernel, which also merges the parts of the rows it split (the part that
+ * finishes last combines them by the rule of mla_combine_splits).
+ * workspace: device memory of at least
  * mla_workspace_size(...) bytes, 256-byte aligned, not shared with a call
  * that may run concurrently.  Returns MLA_OK or a negative mla_status. */
 int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,
@@ -101,9 +106,11 @@ int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,
  * call before any stream capture begins.  A failed look-up returns
  * MLA_ERR_CUDA and is retried by the next call.
  *
- * Limit: batch * sq <= 8192 query rows, and a device with at most 76
- * resident CTA pairs (152 SMs).  Larger requests return MLA_ERR_WORKSPACE
- * before anything is queued.
+ * Limit: batch * sq <= 8192 query rows, and the call's split-KV plan and
+ * partial outputs must fit the 40 MiB array.  They take about 20 MiB on a
+ * GB300 (76 resident CTA pairs on 152 SMs) whatever the batch, and grow
+ * with the number of resident pairs of the device.  A request beyond either
+ * bound returns MLA_ERR_WORKSPACE before anything is queued.
  *
  * Concurrency: every call on one device shares the one scratch array.  Calls
  * queued on the same stream are ordered and safe; calls whose work can
@@ -195,6 +202,11 @@ int mla_up_project_wuv(const uint16_t* latent, const uint16_t* w_uv, int rows, i
 /* Merge split-KV partial results (attention over disjoint token sets):
  *   L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * partial_out_s,
  *   lse = L.
+ * Source: the 128K-token contexts of "DeepSeek R1 Architecture & Deployment
+ * Guide", section 1.1, are far more than one SM pair can stream in time, so
+ * a long row is cut into parts whose softmax results are combined exactly
+ * by this log-sum-exp rule (the decode calls run it on their own splits;
+ * this entry point merges parts a caller produced).
  * partial_out [n_parts, num_heads, 512] fp32 (each part already normalised
  * by its own softmax sum), partial_lse [n_parts, num_heads] fp32,
  * split_indptr [rows+1] int32: row r merges parts [indptr[r], indptr[r+1]).

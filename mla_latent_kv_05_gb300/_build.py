@@ -44,13 +44,18 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None) -> str:
+    """Compile and link the library; returns its path.  `out_dir` (with
+    `extra_flags`, e.g. -D defines) builds a separate copy there, leaving the
+    in-tree library untouched."""
+    if out_dir is None and not extra_flags and not force and up_to_date():
         return LIB_PATH
+    lib_path = LIB_PATH if out_dir is None else os.path.join(out_dir, LIB_NAME)
     nvcc = _nvcc()
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    obj_dir = os.path.join(out_dir or OUT_DIR, "obj")
     os.makedirs(obj_dir, exist_ok=True)
-    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
+    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+                     "-I" + INCLUDE,
                      "--expt-relaxed-constexpr", *extra_flags]
 
     def compile_one(src):
@@ -65,14 +70,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -1,6 +1,6 @@
 // C ABI of the MLA decode library: argument validation, workspace sizing,
 // tensor-map creation and the launch sequence (planner -> paired decode
-// kernel -> split merge), all on the caller's stream.
+// kernel, which also merges the split rows), all on the caller's stream.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -39,12 +39,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (32 tokens), written to shared memory as 8-row x 128-byte swizzle atoms in
 // (row group, chunk, row) order, so consecutive half-page slots form one
 // K-major operand with a constant row-group stride.
-int make_cache_tmap(CUtensorMap* m, const void* cache, int num_pages, unsigned chunks) {
+// `groups` row groups per box: 4 for a half page, 8 for a whole page.
+int make_cache_tmap(CUtensorMap* m, const void* cache, int num_pages, unsigned chunks, unsigned groups = 4) {
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
   cuuint64_t dims[4] = {64, 8, static_cast<cuuint64_t>(kRow / 64), static_cast<cuuint64_t>(num_pages) * (kPage / 8)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(kRow) * 2, 128, static_cast<cuuint64_t>(kRow) * 2 * 8};
-  cuuint32_t box[4] = {64, 8, chunks, 4};
+  cuuint32_t box[4] = {64, 8, chunks, groups};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -87,17 +88,22 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   const WsLayout L = ws_layout(batch, sq, pairs);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  // half pages: chunks 0..4 and 5..8 (score SM), the 8 latent chunks (value SM)
-  CUtensorMap tmap_k, tmap_kb, tmap_v;
+  // half and whole pages of chunks 0..4 and 5..8 (score SM), half pages of
+  // the 8 latent chunks (value SM)
+  CacheMaps maps;
   const bool quant = kind != CacheKind::kBf16;
   if (!quant) {
-    st = make_cache_tmap(&tmap_k, kv_cache, num_pages, 5);
-    if (st == MLA_OK) st = make_cache_tmap(&tmap_kb, kv_cache, num_pages, 4);
-    if (st == MLA_OK) st = make_cache_tmap(&tmap_v, kv_cache, num_pages, 8);
+    st = make_cache_tmap(&maps.k, kv_cache, num_pages, 5);
+    if (st == MLA_OK) st = make_cache_tmap(&maps.k8, kv_cache, num_pages, 5, 8);
+    if (st == MLA_OK) st = make_cache_tmap(&maps.kb, kv_cache, num_pages, 4);
+    if (st == MLA_OK) st = make_cache_tmap(&maps.kb8, kv_cache, num_pages, 4, 8);
+    if (st == MLA_OK) st = make_cache_tmap(&maps.v, kv_cache, num_pages, 8);
     if (st != MLA_OK) return st;
   }
 
-  if (launch_plan(seq_lens, batch, sq, max_pages, ppg, workspace, L, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_plan(seq_lens, batch, sq, max_pages, ppg, workspace, L, reinterpret_cast<__nv_bfloat16*>(out), lse,
+                  stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   DecodeParams p;
   p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
   p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
@@ -108,6 +114,7 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   p.block_table = block_table;
   p.batch = batch;
   p.sq = sq;
+  p.pairs_per_group = ppg;
   p.num_pages = num_pages;
   p.max_pages = max_pages;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -116,11 +123,10 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   p.lse = lse;
   p.ws = static_cast<uint8_t*>(workspace);
   p.L = L;
-  // The three kernels are chained with programmatic dependent launch, so the
-  // attention kernel's prologue overlaps the planner and the merge kernel's
-  // launch overlaps the attention kernel's tail.  A call with the profiling
-  // hook set records its events between the kernels and launches them
-  // without that overlap, so that the events bracket the attention kernel.
+  // The attention kernel is a programmatic dependent of the planner, so its
+  // prologue overlaps the planner.  A call with the profiling hook set
+  // records its events around the attention kernel and launches it without
+  // that overlap, so that the events bracket it alone.
   cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
   g_prof_before = g_prof_after = nullptr;
   const bool pdl = ev0 == nullptr;
@@ -128,10 +134,9 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   cudaError_t le;
   if (kind == CacheKind::kFp8) le = launch_decode_fp8(p, ppg * sq, pdl, stream);
   else if (kind == CacheKind::kFp4) le = launch_decode_fp4(p, ppg * sq, pdl, stream);
-  else le = launch_decode_bf16(tmap_k, tmap_kb, tmap_v, p, ppg * sq, pdl, stream);
+  else le = launch_decode_bf16(maps, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine_plan(workspace, L, batch * sq, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -171,7 +176,7 @@ int static_scratch(void** ptr) {
 constexpr int kMaxTopk = 16384;
 
 // Sparse top-k decode: compact the slot lists, plan the B*Sq query rows as a
-// batch of rows with one query each, gather-attend, merge.
+// batch of rows with one query each, gather-attend (merging split rows).
 int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache, const int32_t* token_slots,
                int batch, int sq, int topk, int num_heads, int num_pages, int page_size, float softmax_scale,
                uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream_ptr) {
@@ -195,7 +200,9 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   if (launch_sparse_prep(token_slots, rows, topk, num_pages * kPage, workspace, L, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   const int32_t* counts = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(workspace) + L.sp_lens);
-  if (launch_plan(counts, rows, 1, max_pages, pairs, workspace, L, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_plan(counts, rows, 1, max_pages, pairs, workspace, L, reinterpret_cast<__nv_bfloat16*>(out), lse,
+                  stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   DecodeParams p;
   memset(&p, 0, sizeof(p));
   p.q_abs = reinterpret_cast<const __nv_bfloat16*>(q_absorbed);
@@ -204,6 +211,7 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   p.block_table = nullptr;
   p.batch = rows;
   p.sq = 1;
+  p.pairs_per_group = pairs;
   p.num_pages = num_pages;
   p.max_pages = max_pages;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -219,12 +227,15 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_decode_sparse(p, pairs, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine_plan(workspace, L, rows, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
 }  // namespace
 
+// Only the C ABI below is exported (the library is built with hidden
+// visibility), so a process may load several copies without their internals
+// binding to each other.
+#pragma GCC visibility push(default)
 extern "C" {
 
 int mla_up_project_wuv(const uint16_t* latent, const uint16_t* w_uv, int rows, int num_heads, int d_v,
@@ -370,3 +381,4 @@ const char* mla_status_string(int code) {
 }
 
 }  // extern "C"
+#pragma GCC visibility pop

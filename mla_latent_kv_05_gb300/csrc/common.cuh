@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "mla_decode.h"
@@ -27,7 +28,7 @@ struct PlanHeader {
   int n_tiles;           // total KV tiles over the batch (longest query)
   int chunk;             // mean pages per pair (information only; the ranges are pair_lo)
   int slots_per_query;   // partial slots of one query index
-  int n_comb;            // rows the merge kernel must write
+  int n_empty;           // rows with no token (written by the planner)
   int pairs_per_group;   // pairs that serve one query index
   int abort_flag;        // set by the first wait that times out; all waits then give up
   int fp8_range;         // FP8/FP4 f16 pass: an input lies outside the f16-exact range (the exact pass recomputes)
@@ -36,7 +37,8 @@ struct PlanHeader {
 
 // Offsets (bytes) of the plan arrays and split partials inside the workspace.
 struct WsLayout {
-  size_t lens, tile_start, row_cost, pair_lo, pair_rank, first_pair, slot_base, comb_row, comb_start, comb_count;
+  size_t lens, tile_start, row_cost, pair_lo, pair_rank, pair_b0, pair_bl, first_pair, slot_base, n_parts,
+      empty_rows, merge_cnt;
   size_t part_lse, part_out;
   size_t sp_lens, sp_slots;   // sparse decode: listed tokens per row, compacted slot lists [rows, topk]
   size_t total;
@@ -58,17 +60,37 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs, int 
   L.row_cost = o;    o = align256(o + sizeof(int) * (batch + 1));
   L.pair_lo = o;     o = align256(o + sizeof(int) * (pg + 1));
   L.pair_rank = o;   o = align256(o + sizeof(int) * (pg + 1));
+  L.pair_b0 = o;     o = align256(o + sizeof(int) * (pg + 1));
+  L.pair_bl = o;     o = align256(o + sizeof(int) * (pg + 1));
   L.first_pair = o;  o = align256(o + sizeof(int) * batch);
   L.slot_base = o;   o = align256(o + sizeof(int) * batch);
-  L.comb_row = o;    o = align256(o + sizeof(int) * batch * sq);
-  L.comb_start = o;  o = align256(o + sizeof(int) * batch * sq);
-  L.comb_count = o;  o = align256(o + sizeof(int) * batch * sq);
+  L.n_parts = o;     o = align256(o + sizeof(int) * batch);
+  L.empty_rows = o;  o = align256(o + sizeof(int) * batch);
+  // merge counters: two passes (the FP8/FP4 exact pass has its own) x split
+  // rows (indexed by their first partial slot)
+  L.merge_cnt = o;   o = align256(o + sizeof(int) * 2 * static_cast<size_t>(L.max_slots));
   L.part_lse = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads);
   L.part_out = o;    o = align256(o + 2 * static_cast<size_t>(L.max_slots) * kHeads * kDc);   // bf16 partials
   L.sp_lens = o;     o = align256(o + (topk > 0 ? sizeof(int) * batch : 0));
   L.sp_slots = o;    o = align256(o + (topk > 0 ? sizeof(int) * static_cast<size_t>(batch) * topk : 0));
   L.total = o;
   return L;
+}
+
+// Launch `kern` and return this launch's own error.  (A <<<>>> launch is
+// checked through cudaGetLastError, which would also return, and clear, an
+// earlier error of the caller's.)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Record the first problem seen (never overwrites an earlier one).
@@ -105,6 +127,33 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Plan
         return false;
       }
     }
+  }
+}
+
+// Time limit of the teardown drains below.  It does not follow
+// MLA_WAIT_TIMEOUT_NS: a drain waits for copies and MMAs that were already
+// issued and complete on their own, whatever happened to the pipeline.
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;   // 200 ms
+
+// Wait until the phase with `parity` of a barrier has completed, i.e. until
+// the copies or MMAs counted on it have landed, ignoring the abort flag.
+// Gives up (recording MLA_STATUS_TIMEOUT) only after kDrainTimeoutNs.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, PlanHeader* hdr) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > kDrainTimeoutNs) {
+      set_status(&hdr->status, MLA_STATUS_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Spin for `ns` nanoseconds (the abort path's grace for stores another CTA
+// of the cluster issued into this one's shared memory and cannot track).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (ptx::globaltimer() - t0 < ns) {
   }
 }
 

@@ -35,12 +35,13 @@
 // each other's row-group sequence at a constant stride (5 KiB, 4 KiB), so a
 // block is one 96-row K-major operand, whatever pages the slots came from.
 // S consumes the A part first and releases it, so the next tile's A part
-// loads while S reads the B part.  The A parts are loaded by the score SM,
-// the B parts by the value SM's TMA unit (multicast to the score SM alone),
-// because each TMA operation costs the issuing SM about 225 ns.  The value
-// SM keeps half-page V slots (atoms at 1 KiB per chunk, 8 KiB per row
-// group), read as MN-major operands 16 tokens at a time.  Both ranks read
-// every half page; the second read is an L2 hit.
+// loads while S reads the B part.  Each SM's TMA loads land only in its own
+// shared memory.  Each TMA operation costs the issuing SM about 225 ns, so
+// the score SM loads two adjacent slots that hold the halves of one page with
+// one whole-page box (two operations per part and tile instead of three).
+// The value SM keeps half-page V slots (atoms at 1 KiB per chunk, 8 KiB per
+// row group), read as MN-major operands 16 tokens at a time.  Both ranks
+// read every half page; the second read is an L2 hit.
 //
 // The FP8 cache is bulk-copied as raw half pages by both SMs, and each SM
 // dequantises what its own MMAs read (score SM: all nine chunks into the
@@ -156,7 +157,8 @@ enum Bar {
   QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY, LSUM,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
   RAWFULL = MBEMPTY + kMailSlots, RAWEMPTY = RAWFULL + kMaxRaw,
-  NBAR = RAWEMPTY + kMaxRaw
+  DRAIN = RAWEMPTY + kMaxRaw,   // the MMA issuer's last commit, waited for at teardown
+  NBAR
 };
 constexpr uint32_t kMiscTmem = kMiscBar + NBAR * 8;
 constexpr uint32_t kMiscBytes = kMiscTmem + 16;
@@ -202,16 +204,10 @@ struct Segment {
 struct SegWalker {
   const int* tile_start;
   int batch, b, lo, hi;
-  __device__ void init(const int* ts, int nb, int lo_, int hi_) {
+  // b0: the row holding page lo (the planner's pair_b0)
+  __device__ void init(const int* ts, int nb, int lo_, int hi_, int b0) {
     tile_start = ts; batch = nb; lo = lo_; hi = hi_;
-    b = 0;
-    if (lo >= hi) { b = nb; return; }
-    int l = 0, r = nb - 1;            // largest b with ts[b] <= lo
-    while (l < r) {
-      const int mid = (l + r + 1) >> 1;
-      if (__ldg(ts + mid) <= lo) l = mid; else r = mid - 1;
-    }
-    b = l;
+    b = lo >= hi ? nb : b0;
   }
   __device__ bool next(Segment& s) {
     while (b < batch) {
@@ -475,6 +471,150 @@ __device__ __forceinline__ void load_q_rolled(const uint8_t* qa, const uint8_t* 
   }
 }
 
+// ------------------------------------------------------------ split-row merge
+// A row cut into P > 1 parts is merged inside the attention kernel.  Every
+// part writes its normalised bf16 partial (rank 0's epilogue warps) and its
+// lse (rank 1's first softmax group), and each of those warps then adds one
+// to the row's counter with a release.  Parts 0 .. P-2 of a row always end
+// their pair's page range (the row goes on into the next pair), so they run
+// last in their pairs; after their own part they merge a slice of the 128
+// heads each (both SMs of the pair, one warp per head), once the counter
+// shows every part written; every warp of both CTAs joins in (a merger's
+// roles are all done by then).  Part P-1 never waits, and no part waits for
+// a merger, so every wait ends.  The parts are summed in slot order, so the
+// result does not depend on which part finishes first.
+// The warp's writes (and those it has acquired) are visible GPU-wide before
+// the row's counter moves.
+__device__ __forceinline__ void count_written(uint32_t* cnt, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) ptx::red_release_gpu_add(cnt, 1u);
+}
+
+// Wait (warp-uniformly, bounded) until the counter reaches `want`.
+__device__ __forceinline__ bool wait_count(const uint32_t* cnt, uint32_t want, PlanHeader* hdr) {
+  if (__all_sync(0xffffffffu, ptx::ld_acquire_gpu(cnt) >= want)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(128);   // the warps of this SM that still work get the issue slots
+    if (__all_sync(0xffffffffu, ptx::ld_acquire_gpu(cnt) >= want)) return true;
+    if ((n & 63u) == 0) {
+      bool give_up = read_status(&hdr->abort_flag) != 0;
+      if (!give_up && ptx::globaltimer() - t0 > MLA_WAIT_TIMEOUT_NS) {
+        set_status(&hdr->status, MLA_STATUS_TIMEOUT);
+        atomicExch(&hdr->abort_flag, 1);
+        give_up = true;
+      }
+      if (__any_sync(0xffffffffu, give_up)) return false;
+    }
+  }
+}
+
+// Merge heads [h_begin, h_end) of a split row from its `parts` partials at
+// slots slot0 ..: warp g of nw takes heads h_begin + g, + nw, ..., kHB at a
+// time so that their loads are in flight together; lane = 16 latent columns
+// (one 32-byte sector of a partial row).  L = max lse, weights exp(lse - L),
+// out = sum_s w_s o_s / sum_s w_s, lse = L + ln sum_s w_s.
+// kHB heads per round (more in flight, more registers).
+template <int kHB>
+__device__ __forceinline__ void merge_heads(const __nv_bfloat16* part_out, const float* part_lse, int slot0, int parts,
+                                         int h_begin, int h_end, int g, int nw, int lane, __nv_bfloat16* out_row,
+                                         float* lse_row) {
+  auto lse_at = [&](int s, int h) { return __ldcg(part_lse + static_cast<size_t>(slot0 + s) * kHeads + h); };
+  auto row_at = [&](int s, int h) {
+    return part_out + (static_cast<size_t>(slot0 + s) * kHeads + h) * kDc + 16 * lane;
+  };
+#pragma unroll 1
+  for (int h0 = h_begin + g; h0 < h_end; h0 += kHB * nw) {
+    int hh[kHB];
+    bool on[kHB];
+#pragma unroll
+    for (int j = 0; j < kHB; ++j) {
+      hh[j] = h0 + j * nw;
+      on[j] = hh[j] < h_end;
+    }
+    // Issued together: every lane's first lse (part `lane`) and the first
+    // two parts' values, so that a two-part row takes one round trip.
+    float v0[kHB];
+    uint32_t x[2][kHB][8];
+#pragma unroll
+    for (int j = 0; j < kHB; ++j) {
+      v0[j] = (lane < parts && on[j]) ? lse_at(lane, hh[j]) : -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t < parts && on[j]) {
+          ptx::ld_global_cg_v8(row_at(t, hh[j]), x[t][j]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[t][j][e] = 0u;
+        }
+      }
+    }
+    float L[kHB], sum[kHB], acc[kHB][16];
+#pragma unroll
+    for (int j = 0; j < kHB; ++j) {
+      L[j] = v0[j];
+      for (int s = lane + 32; s < parts; s += 32)
+        if (on[j]) L[j] = fmaxf(L[j], lse_at(s, hh[j]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L[j] = fmaxf(L[j], __shfl_xor_sync(0xffffffffu, L[j], o));
+      sum[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[j][e] = 0.f;
+    }
+    for (int s0 = 0; s0 < parts; s0 += 32) {
+      // lane u: the weight of part s0 + u
+      float wl[kHB];
+#pragma unroll
+      for (int j = 0; j < kHB; ++j) {
+        const float v = s0 == 0 ? v0[j] : ((s0 + lane < parts && on[j]) ? lse_at(s0 + lane, hh[j]) : -INFINITY);
+        wl[j] = v == -INFINITY ? 0.f : __expf(v - L[j]);
+      }
+      const int n = min(32, parts - s0);
+      for (int u = 0; u < n; u += 2) {
+        if (s0 + u > 0) {
+#pragma unroll
+          for (int j = 0; j < kHB; ++j) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (u + t < n && on[j]) {
+                ptx::ld_global_cg_v8(row_at(s0 + u + t, hh[j]), x[t][j]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[t][j][e] = 0u;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+          for (int j = 0; j < kHB; ++j) {
+            const float w = u + t < n && on[j] ? __shfl_sync(0xffffffffu, wl[j], u + t) : 0.f;
+            sum[j] += w;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[t][j][e]));
+              acc[j][2 * e] = fmaf(w, f.x, acc[j][2 * e]);
+              acc[j][2 * e + 1] = fmaf(w, f.y, acc[j][2 * e + 1]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kHB; ++j) {
+      if (!on[j]) continue;
+      const float inv = sum[j] > 0.f ? 1.f / sum[j] : 0.f;
+      uint32_t o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = pack_bf16x2(acc[j][2 * e] * inv, acc[j][2 * e + 1] * inv);
+      ptx::st_global_v8(out_row + static_cast<size_t>(hh[j]) * kDc + 16 * lane, o);
+      if (lane == 0) lse_row[hh[j]] = sum[j] > 0.f ? L[j] + logf(sum[j]) : -INFINITY;
+    }
+  }
+}
+
 }  // namespace dk
 
 // kMode 0: bf16 cache via TMA; 1: FP8 cache via bulk copies + dequant to
@@ -483,8 +623,7 @@ __device__ __forceinline__ void load_q_rolled(const uint8_t* qa, const uint8_t* 
 // over the bf16 cache (rows gathered by listed slot with 16-byte cp.async)
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dk::Cfg<kMode>::kThreads, 1)
-mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_kb,
-                       const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParams p) {
   using namespace dk;
   using C = Cfg<kMode>;
   constexpr int TH = C::kTileHalves;            // half pages per tile
@@ -520,6 +659,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const int* slot_base = reinterpret_cast<const int*>(p.ws + p.L.slot_base);
   float* part_lse = reinterpret_cast<float*>(p.ws + p.L.part_lse);
   __nv_bfloat16* part_out = reinterpret_cast<__nv_bfloat16*>(p.ws + p.L.part_out);
+  const int* n_parts = reinterpret_cast<const int*>(p.ws + p.L.n_parts);
+  uint32_t* merge_cnt = reinterpret_cast<uint32_t*>(p.ws + p.L.merge_cnt);
   auto BAR = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
   // physical page of row-local half page hp of batch row b (or -1 if out of range)
   auto half_page = [&](int b, int hp) -> int {
@@ -559,6 +700,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       ptx::mbar_init(BAR(RAWFULL + s), 1);
       ptx::mbar_init(BAR(RAWEMPTY + s), kQuant ? dq : 1u);
     }
+    ptx::mbar_init(BAR(DRAIN), 1);
     ptx::fence_barrier_init();
   }
   if (warp == 2) {
@@ -566,8 +708,14 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     ptx::tmem_relinquish();
   }
   if (kMode == 0 && warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(rank == 1 ? &tmap_k : &tmap_v);
-    ptx::prefetch_tmap(&tmap_kb);
+    if (rank == 1) {
+      ptx::prefetch_tmap(&maps.k);
+      ptx::prefetch_tmap(&maps.k8);
+      ptx::prefetch_tmap(&maps.kb);
+      ptx::prefetch_tmap(&maps.kb8);
+    } else {
+      ptx::prefetch_tmap(&maps.v);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -580,13 +728,14 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   ptx::grid_dep_launch();   // the merge kernel may begin launching
   if (threadIdx.x == 0 && !smem_ok) set_status(&hdr->status, MLA_ERR_UNSUPPORTED);
 
-  const int ppg = hdr->pairs_per_group;
+  const int ppg = p.pairs_per_group;
   const int group = static_cast<int>(pair) / ppg;     // query index i served by this pair
   const int pl = static_cast<int>(pair) % ppg;
   const int spq = hdr->slots_per_query;
   const int* pair_lo = reinterpret_cast<const int*>(p.ws + p.L.pair_lo);
   const int* pair_rank = reinterpret_cast<const int*>(p.ws + p.L.pair_rank);   // non-empty pairs before p
   const int lo = pair_lo[pl], hi = pair_lo[pl + 1];     // this pair's page range (cost-balanced by the planner)
+  const int b0 = reinterpret_cast<const int*>(p.ws + p.L.pair_b0)[pl];   // the row holding page lo
   const int sq = p.sq;
   // the exact FP8 pass after an f16 pass runs only if that pass flagged an
   // input outside the f16-exact range
@@ -605,7 +754,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     // async proxies after their waits.  Tokens past the row's count are not
     // copied (the softmax masks them; the value SM zeroes their V rows).
     const int gw = warp == 0 ? 0 : warp - 1;
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
     Segment sg;
     int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
     int vs = 0; uint32_t vphase = 0;      // rank 0: V ring head
@@ -683,11 +832,12 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         }
       }
     }
+    ptx::cp_async_wait_all();   // (after an abort) no copy of this thread may land after the CTA left
   } else if (kMode != 3 && active && warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_normal();
-      SegWalker w; w.init(tile_start, p.batch, lo, hi);
+      SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
       Segment sg;
       int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
       int vs = 0; uint32_t vphase = 0;      // rank 0: V slot
@@ -695,6 +845,20 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
       const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
       volatile uint32_t* raw_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffRawFlag);
+      // Full barriers this thread armed for copies (bit i: ring slot i, see
+      // full_bar below) and the phase parity of each one's last arming: at
+      // the end every such phase is waited for, so that no copy lands after
+      // the CTA has left (which matters only when a wait gave up).
+      uint32_t armed = 0, armed_par = 0;
+      auto arm = [&](int bit, uint32_t phase) {
+        armed |= 1u << bit;
+        armed_par = (armed_par & ~(1u << bit)) | (phase << bit);
+      };
+      auto full_bar = [&](int bit) -> uint32_t {
+        if (kMode != 0) return BAR(RAWFULL + bit);
+        if (rank == 0) return BAR(VFULL + bit);
+        return bit < 2 ? BAR(KFULL + bit) : BAR(KFULLB + bit - 2);
+      };
       bool ok = true;
       while (ok && w.next(sg)) {
         const int hp_end = 2 * sg.t1;
@@ -719,7 +883,12 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               // A tile buffer holds the tile's chunks 0..4 (A part) and
               // chunks 5..8 (B part) of every half page in two blocks.  S
               // consumes the A part first, so the next tile's A part is
-              // refilled while S still reads the B part.
+              // refilled while S still reads the B part.  Two adjacent slots
+              // that hold the two halves of one page take one whole-page box
+              // (8 row groups land as the two slots' row groups 0..7), so a
+              // 96-token tile costs two TMA operations per part, not three:
+              // each operation costs the issuing SM's TMA unit a roughly
+              // fixed time, whatever its size.
               const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);
               int wq[TH];
 #pragma unroll
@@ -730,12 +899,26 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               }
               if (!wait_bounded<true>(BAR(KEMPTY + kb), kphase ^ 1u, hdr)) { ok = false; break; }
               ptx::mbar_arrive_expect_tx(BAR(KFULL + kb), static_cast<uint32_t>(nh) * kKA);
+              arm(kb, kphase);
 #pragma unroll
               for (int j = 0; j < TH; ++j) {
                 if (j >= nh) break;
-                ptx::tma_load_4d(tbase + static_cast<uint32_t>(j) * kKA, &tmap_k, BAR(KFULL + kb), 0, 0, 0, wq[j], pol);
+                const bool whole = ((h0 + j) & 1) == 0 && j + 1 < nh;
+                if (j > 0 && ((h0 + j) & 1) == 1) continue;   // second half, loaded with the first
+                ptx::tma_load_4d(tbase + static_cast<uint32_t>(j) * kKA, whole ? &maps.k8 : &maps.k, BAR(KFULL + kb),
+                                 0, 0, 0, wq[j], pol);
               }
-              // (the B parts are issued by rank 0: its TMA unit is less busy)
+              if (!wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
+              ptx::mbar_arrive_expect_tx(BAR(KFULLB + kb), static_cast<uint32_t>(nh) * kKB);
+              arm(2 + kb, kphase);
+#pragma unroll
+              for (int j = 0; j < TH; ++j) {
+                if (j >= nh) break;
+                const bool whole = ((h0 + j) & 1) == 0 && j + 1 < nh;
+                if (j > 0 && ((h0 + j) & 1) == 1) continue;
+                ptx::tma_load_4d(tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(j) * kKB,
+                                 whole ? &maps.kb8 : &maps.kb, BAR(KFULLB + kb), 0, 0, 5, wq[j], pol);
+              }
               kb ^= 1;
               if (kb == 0) kphase ^= 1u;
             } else {
@@ -746,7 +929,8 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                 const int hp = h0 + j, page = pages[j];
                 const int wq = (page < 0 ? p.num_pages : page) * 8 + (hp & 1) * 4;
                 ptx::mbar_arrive_expect_tx(BAR(VFULL + vs), kVSlot);
-                ptx::tma_load_4d(sbase + static_cast<uint32_t>(vs) * kVSlot, &tmap_v, BAR(VFULL + vs), 0, 0, 0, wq,
+                arm(vs, vphase);
+                ptx::tma_load_4d(sbase + static_cast<uint32_t>(vs) * kVSlot, &maps.v, BAR(VFULL + vs), 0, 0, 0, wq,
                                  pol);
                 if (++vs == kVSlots) { vs = 0; vphase ^= 1u; }
               }
@@ -760,6 +944,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
               const int hp = h0 + j, page = pages[j];
               if (page < 0) set_status(&hdr->status, MLA_STATUS_BAD_PAGE);
               raw_flag[rs] = page < 0 ? 1u : 0u;
+              arm(rs, rphase);
               if (page < 0) {
                 ptx::mbar_arrive(BAR(RAWFULL + rs));
               } else {
@@ -788,6 +973,9 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
           }
         }
       }
+#pragma unroll 1
+      for (int i = 0; i < 8; ++i)
+        if ((armed >> i) & 1u) wait_drain(full_bar(i), (armed_par >> i) & 1u, hdr);
     }
   } else if (kQuant && active && (warp >= 8 || (warp == 2 && rank == 1))) {
     // ------------------------------------------------------------ FP8 dequant
@@ -801,7 +989,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     const volatile uint32_t* raw_flag = reinterpret_cast<const volatile uint32_t*>(smem + kOffRawFlag);
     const uint32_t raw_off = rank == 1 ? C::kOffRaw1 : C::kOffRaw0;
     const int n_raw = rank == 1 ? C::kRaw1 : C::kRaw0;
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
     Segment sg;
     int kb = 0; uint32_t kphase = 0;      // rank 1: K tile buffer
     int vs = 0; uint32_t vphase = 0;      // rank 0: V slot
@@ -864,63 +1052,25 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         if (kb == 0) kphase ^= 1u;
       }
     }
-  } else if (kMode == 0 && active && warp == 3 && rank == 0) {
-    // ------------------------------------------------------------ B-part loader for rank 1 (bf16)
-    // The B part (chunks 5..8) of each of rank 1's K tiles, loaded by this
-    // CTA's TMA unit as a multicast whose only destination is rank 1: the
-    // data and the complete_tx land at the same offsets there.  Rank 1's S
-    // commits the release of a B part to this CTA (KEMPTYB).
-    if (lane == 0) {
-      const uint64_t pol = ptx::policy_evict_normal();
-      SegWalker w; w.init(tile_start, p.batch, lo, hi);
-      Segment sg;
-      int kb = 0; uint32_t kphase = 0;
-      bool ok = true;
-      while (ok && w.next(sg)) {
-        const int hp_end = 2 * sg.t1;
-        int next_pages[TH];
-#pragma unroll
-        for (int j = 0; j < TH; ++j) next_pages[j] = 2 * sg.t0 + j < hp_end ? half_page(sg.b, 2 * sg.t0 + j) : 0;
-        for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
-          const int nh = min(TH, hp_end - h0);
-          int wq[TH];
-#pragma unroll
-          for (int j = 0; j < TH; ++j) {
-            wq[j] = (next_pages[j] < 0 ? p.num_pages : next_pages[j]) * 8 + ((h0 + j) & 1) * 4;
-            next_pages[j] = h0 + TH + j < hp_end ? half_page(sg.b, h0 + TH + j) : 0;
-          }
-          if (!wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx_remote(ptx::mapa(BAR(KFULLB + kb), 1), static_cast<uint32_t>(nh) * kKB);
-          const uint32_t tbase = sbase + static_cast<uint32_t>(kb) * (TH * kKSlot);   // rank 1's tile buffer
-#pragma unroll
-          for (int j = 0; j < TH; ++j) {
-            if (j >= nh) break;
-            ptx::tma_load_4d_mc(tbase + static_cast<uint32_t>(TH) * kKA + static_cast<uint32_t>(j) * kKB, &tmap_kb,
-                                BAR(KFULLB + kb), 0, 0, 5, wq[j], static_cast<uint16_t>(2u), pol);
-          }
-          kb ^= 1;
-          if (kb == 0) kphase ^= 1u;
-        }
-      }
-      // rank 1's last S commits arrive here: wait for them before this CTA may leave
-      for (int s = 0; s < 2 && ok; ++s) {
-        ok = wait_bounded<true>(BAR(KEMPTYB + kb), kphase ^ 1u, hdr);
-        kb ^= 1;
-        if (kb == 0) kphase ^= 1u;
-      }
-    }
   } else if (active && warp == 1 && rank == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
     // One tile = TH adjacent half-page slots = one kN-row K-major operand;
     // K-step k reads chunk k/4 at byte 32*(k%4) inside the 8-row atoms.
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
     Segment sg;
     int kb = 0; uint32_t kphase = 0;
     int sb = 0; uint32_t sphase = 0;
     uint32_t qphase = 0;
-    bool ok = true;
+    bool ok = true, issued = false;
+#ifdef MLA_TEST_STALL_WAIT
+    // Test builds only: a wait on a barrier that nothing arrives on before
+    // the end of the kernel, so that the wait limit (MLA_WAIT_TIMEOUT_NS) runs
+    // out and every role leaves through the abort path.
+    ok = wait_warp<false>(BAR(DRAIN), 0u, hdr);
+#endif
     while (ok && w.next(sg)) {
       if (!wait_warp<false>(BAR(QREADY), qphase, hdr)) break;
+      issued = true;
       qphase ^= 1u;
       const int hp_end = 2 * sg.t1;
       for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
@@ -952,9 +1102,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             for (int k = 20; k < kRow / 16; ++k)
               ptx::mma_ts(d, tmem + kQCol + 8u * k,
                           db + static_cast<uint64_t>((((k >> 2) - 5) * kAtom + (k & 3) * 32) >> 4), kIdescS, 1u);
-            // bf16: rank 0 issues the B loads; sparse: this CTA gathers them
-            if constexpr (kMode == 3) ptx::mma_commit(BAR(KEMPTYB + kb));
-            else ptx::mma_commit_mc(BAR(KEMPTYB + kb), static_cast<uint16_t>(1u));
+            ptx::mma_commit(BAR(KEMPTYB + kb));
             ptx::mma_commit(BAR(SFULL + sb));
           }
         } else if (lane == 0) {
@@ -977,19 +1125,26 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         if (++sb == 2) { sb = 0; sphase ^= 1u; }
       }
     }
+    // every MMA this thread issued completes before the CTA may leave
+    if (issued && lane == 0) {
+      ptx::mma_commit(BAR(DRAIN));
+      wait_drain(BAR(DRAIN), 0u, hdr);
+    }
+    __syncwarp();
   } else if (active && warp == 1 && rank == 0) {
     // ------------------------------------------------------------ O += P V issuer
     // Per half page of the tile: two K-steps of 16 tokens (two row groups of
     // the V slot each), two N=256 halves of the latent columns per step.
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
     Segment sg;
     int vs = 0; uint32_t vphase = 0;
     int ps = 0; uint32_t pphase = 0;
     uint32_t corr_phase = 0, oe_phase = 0;
-    bool first_seg = true, ok = true;
+    bool first_seg = true, ok = true, issued = false;
     volatile uint32_t* req_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffReq);
     const volatile float* alpha_buf = reinterpret_cast<const volatile float*>(smem + kOffAlpha);
     while (ok && w.next(sg)) {
+      issued = true;
       const int len_i = lens[sg.b] - (sq - 1 - group);
       const int hp_end = 2 * sg.t1;
       for (int h0 = 2 * sg.t0; h0 < hp_end && ok; h0 += TH) {
@@ -1061,6 +1216,13 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       }
       first_seg = false;
     }
+    // every MMA (and the commits to rank 1) this thread issued completes
+    // before the CTA may leave
+    if (issued && lane == 0) {
+      ptx::mma_commit(BAR(DRAIN));
+      wait_drain(BAR(DRAIN), 0u, hdr);
+    }
+    __syncwarp();
   } else if (active && warp >= 4 && warp < 4 + 4 * kSG && rank == 1) {
     // ------------------------------------------------------------ softmax (thread = head)
     // bf16 (two groups): group 0 (warps 4..7) turns columns [0, kHC) of each
@@ -1072,7 +1234,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     const int h = (threadIdx.x - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     volatile float* l_part = reinterpret_cast<volatile float*>(smem + C::kOffMisc + kMiscLPart);
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
     Segment sg;
     int sb = 0; uint32_t sphase = 0;
     int ps = 0; uint32_t pphase = 0;
@@ -1214,8 +1376,13 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const int slot = split ? group * spq + slot_base[sg.b] + (pair_rank[pl] - pair_rank[first_pair[sg.b]]) : -1;
         const float lse_v = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -INFINITY;
         const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;   // correctly rounded, as 1/l
-        if (split) part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
-        else p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
+        if (split) {
+          part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
+          count_written(merge_cnt + static_cast<size_t>(p.fp8_fallback) * p.L.max_slots + group * spq + slot_base[sg.b],
+                        lane);
+        } else {
+          p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
+        }
         if (!wait_warp<true>(BAR(MBEMPTY + ms), mphase ^ 1u, hdr)) { ok = false; break; }
         const uint32_t mbfull = ptx::mapa(BAR(MBFULL + ms), 0);
         ptx::mbar_arrive_expect_tx_remote(mbfull, 4u);
@@ -1243,7 +1410,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     const int h = (threadIdx.x - 128) & 127;
     const int c0 = kEpChunks * ((warp - 4) >> 2);     // first 32-column chunk of this warp
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    SegWalker w; w.init(tile_start, p.batch, lo, hi);
+    SegWalker w; w.init(tile_start, p.batch, lo, hi, b0);
     Segment sg;
     uint32_t req_phase = 0, of_phase = 0;
     int ms = 0; uint32_t mphase = 0;
@@ -1302,11 +1469,12 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       if (!wait_warp<true>(BAR(MBFULL + ms), mphase, hdr)) { ok = false; break; }
       const float inv_l = mail[ms * 128 + h];
       // out = bf16(O / l): into the output row, or (split rows) into the
-      // row's partial slot, which the merge kernel combines
-      const bool split = slot_base[sg.b] >= 0;
-      __nv_bfloat16* dst =
-          split ? part_out + (static_cast<size_t>(group * spq + slot_base[sg.b] + (pair_rank[pl] - pair_rank[first_pair[sg.b]])) * kHeads + h) * kDc
-                : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
+      // row's partial slot, counted written afterwards (the merge below)
+      const int parts = n_parts[sg.b];
+      const int slot0 = parts > 1 ? group * spq + slot_base[sg.b] : 0;        // the row's first partial slot
+      const int mine = parts > 1 ? pair_rank[pl] - pair_rank[first_pair[sg.b]] : 0;
+      __nv_bfloat16* dst = parts > 1 ? part_out + (static_cast<size_t>(slot0 + mine) * kHeads + h) * kDc
+                                     : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
 #pragma unroll 1
       for (int cc = c0; cc < c0 + kEpChunks; ++cc) {
         uint32_t r[32];
@@ -1318,6 +1486,7 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         ptx::st_global_v8(dst + cc * 32, o);          // whole 32-byte sectors
         ptx::st_global_v8(dst + cc * 32 + 16, o + 8);
       }
+      if (parts > 1) count_written(merge_cnt + static_cast<size_t>(p.fp8_fallback) * p.L.max_slots + slot0, lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive(BAR(OEMPTY));
       __syncwarp();
@@ -1326,7 +1495,32 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     }
   }
 
+  // ------------------------------------------------------------ split-row merge
+  // Every warp of both CTAs, once its role is done: if this pair's last
+  // segment is part k < P-1 of a split row, merge heads [128k/(P-1),
+  // 128(k+1)/(P-1)) of that row (see merge_heads).
+  if (active && lo < hi && read_status(&hdr->abort_flag) == 0) {
+    const int bl = reinterpret_cast<const int*>(p.ws + p.L.pair_bl)[pl];   // the row holding page hi - 1
+    const int parts = n_parts[bl];
+    const int mine = parts > 1 ? pair_rank[pl] - pair_rank[first_pair[bl]] : 0;
+    if (parts > 1 && mine < parts - 1) {
+      const int slot0 = group * spq + slot_base[bl];
+      const int row = bl * sq + group;
+      const int nwarps = static_cast<int>(blockDim.x >> 5);
+      const uint32_t* cnt = merge_cnt + static_cast<size_t>(p.fp8_fallback) * p.L.max_slots + slot0;
+      if (wait_count(cnt, static_cast<uint32_t>(parts * (C::kEpWarps + 4)), hdr))
+        merge_heads<C::kThreads <= 384 ? 3 : 1>(part_out, part_lse, slot0, parts, kHeads * mine / (parts - 1), kHeads * (mine + 1) / (parts - 1),
+                    static_cast<int>(rank) * nwarps + warp, 2 * nwarps, lane,
+                    p.out + static_cast<size_t>(row) * kHeads * kDc, p.lse + static_cast<size_t>(row) * kHeads);
+    }
+  }
+
   // ------------------------------------------------------------ teardown
+  // After a wait gave up, the partner CTA's st.async stores into this CTA's
+  // shared memory may still be in flight, and nothing counts them any more:
+  // give them time to land (they take about a microsecond) before the
+  // cluster may leave.  Copies and MMAs this CTA issued were drained above.
+  if (read_status(&hdr->abort_flag) != 0) spin_ns(20000);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::cluster_sync();
@@ -1336,14 +1530,19 @@ mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   }
 }
 
+namespace {
+
 // Host-side launcher.  kMode 0: bf16 cache through the 4-D tensor maps
-// (half-page boxes: chunks 0..4 and 5..8 for rank 1, eight for rank 0);
-// 1 and 2: FP8 cache, 4 and 5: FP4 cache (p.kv_quant; tensor maps unused;
-// 2 and 5 take f16 operands, 1 and 4 bf16);
-// 3: sparse gather from the bf16 cache.
+// (half- and whole-page boxes of chunks 0..4 and 5..8 for rank 1, half-page
+// boxes of the eight latent chunks for rank 0); 1 and 2: FP8 cache, 4 and 5:
+// FP4 cache (p.kv_quant; tensor maps unused; 2 and 5 take f16 operands, 1
+// and 4 bf16); 3: sparse gather from the bf16 cache.  It lives in an
+// unnamed namespace so that its per-device static is this library's own:
+// a function-local static of a template with external linkage is one
+// object per process, shared by every loaded copy of the library.
 template <int kMode>
-cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
-                               const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
+cudaError_t launch_decode_mode(const CacheMaps& maps, const DecodeParams& p, int n_pairs, bool pdl,
+                               cudaStream_t stream) {
   auto kern = mla_decode_pair_kernel<kMode>;
   static int configured_device = -1;
   int dev = 0;
@@ -1363,44 +1562,46 @@ cudaError_t launch_decode_mode(const CUtensorMap& tmap_k, const CUtensorMap& tma
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmap_k, tmap_kb, tmap_v, p);
+  return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 
-cudaError_t launch_decode_bf16(const CUtensorMap& tmap_k, const CUtensorMap& tmap_kb, const CUtensorMap& tmap_v,
-                               const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
-  return launch_decode_mode<0>(tmap_k, tmap_kb, tmap_v, p, n_pairs, pdl, stream);
+}  // namespace
+
+cudaError_t launch_decode_bf16(const CacheMaps& maps, const DecodeParams& p, int n_pairs, bool pdl,
+                               cudaStream_t stream) {
+  return launch_decode_mode<0>(maps, p, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
-  CUtensorMap unused;
+  CacheMaps unused;
   memset(&unused, 0, sizeof(unused));
   // the f16-operand pass, then the exact bf16-operand pass, which returns at
   // once unless the first pass flagged an input outside the f16-exact range
   DecodeParams q = p;
   q.fp8_fallback = 0;
-  cudaError_t e = launch_decode_mode<2>(unused, unused, unused, q, n_pairs, pdl, stream);
+  cudaError_t e = launch_decode_mode<2>(unused, q, n_pairs, pdl, stream);
   if (e != cudaSuccess) return e;
   q.fp8_fallback = 1;
-  return launch_decode_mode<1>(unused, unused, unused, q, n_pairs, pdl, stream);
+  return launch_decode_mode<1>(unused, q, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_fp4(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
-  CUtensorMap unused;
+  CacheMaps unused;
   memset(&unused, 0, sizeof(unused));
   // as for FP8: the f16-operand pass, then the exact bf16-operand pass,
   // which returns at once unless the first pass flagged an input
   DecodeParams q = p;
   q.fp8_fallback = 0;
-  cudaError_t e = launch_decode_mode<5>(unused, unused, unused, q, n_pairs, pdl, stream);
+  cudaError_t e = launch_decode_mode<5>(unused, q, n_pairs, pdl, stream);
   if (e != cudaSuccess) return e;
   q.fp8_fallback = 1;
-  return launch_decode_mode<4>(unused, unused, unused, q, n_pairs, pdl, stream);
+  return launch_decode_mode<4>(unused, q, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
-  CUtensorMap unused;
+  CacheMaps unused;
   memset(&unused, 0, sizeof(unused));
-  return launch_decode_mode<3>(unused, unused, unused, p, n_pairs, pdl, stream);
+  return launch_decode_mode<3>(unused, p, n_pairs, pdl, stream);
 }
 
 int decode_max_pairs() {

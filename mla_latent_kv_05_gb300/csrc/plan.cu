@@ -1,7 +1,9 @@
 // Split-KV planner: turns seq_lens (on the device, no host sync) into an even
-// partition of KV tiles over the persistent CTA pairs, the partial-output
-// slots of rows that end up split, and the list of rows the merge kernel
-// writes.  One CTA of 1024 threads.
+// partition of KV tiles over the persistent CTA pairs and the partial-output
+// slots of rows that end up split.  One CTA of 1024 threads; the arrays it
+// searches are mirrored in shared memory, because a chain of dependent
+// global reads would sit on the call's critical path (the attention kernel
+// waits for this grid).
 //
 // Partition: every batch row b has n_b = ceil(seq_len_b / 64) pages.  The
 // rows' pages are laid end to end (prefix sums tile_start) and cut into one
@@ -12,8 +14,12 @@
 // query index i < Sq has its own group of pairs with the identical
 // partition, so the groups read the same pages at about the same time and
 // share them in L2.  A row covered by one pair is written straight to `out`;
-// a row covered by k > 1 pairs gets k partial slots (per query index) and a
-// merge entry.
+// a row covered by k > 1 pairs gets k partial slots (per query index), and
+// the attention kernel merges them (the part that finishes last does).  The
+// planner zeroes the merge counters and writes the rows that have no token
+// (out = 0, lse = -inf), which the attention kernel never visits.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace mla {
@@ -52,33 +58,50 @@ __device__ int block_exclusive_scan(int v, int* smem_warp, int* total) {
   return warp_excl + x - v;
 }
 
+// Rows whose planner arrays (tile starts and costs) are kept in shared
+// memory while the planner searches them; larger batches search the global
+// copies instead (the same result, with longer dependent reads).
+constexpr int kPlanSmemRows = 4096;
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens, int batch, int sq,
                                                     int max_pages, int pairs_per_group,
-                                                    uint8_t* __restrict__ ws, WsLayout L) {
+                                                    uint8_t* __restrict__ ws, WsLayout L,
+                                                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   __shared__ int s_warp[32];
   __shared__ int s_chunk;
+  // dynamic: pair_lo and pair_rank mirrors [ppg + 1] each, then (batch <=
+  // kPlanSmemRows) tile_start and row_cost mirrors [batch + 1] each
+  extern __shared__ int s_dyn[];
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
   int* lens = reinterpret_cast<int*>(ws + L.lens);
   int* tile_start = reinterpret_cast<int*>(ws + L.tile_start);
-  int* row_cost = reinterpret_cast<int*>(ws + L.row_cost);
   int* pair_lo = reinterpret_cast<int*>(ws + L.pair_lo);
   int* pair_rank = reinterpret_cast<int*>(ws + L.pair_rank);
+  int* pair_b0 = reinterpret_cast<int*>(ws + L.pair_b0);
+  int* pair_bl = reinterpret_cast<int*>(ws + L.pair_bl);
   int* first_pair = reinterpret_cast<int*>(ws + L.first_pair);
   int* slot_base = reinterpret_cast<int*>(ws + L.slot_base);
-  int* comb_row = reinterpret_cast<int*>(ws + L.comb_row);
-  int* comb_start = reinterpret_cast<int*>(ws + L.comb_start);
-  int* comb_count = reinterpret_cast<int*>(ws + L.comb_count);
+  int* n_parts = reinterpret_cast<int*>(ws + L.n_parts);
+  int* empty_rows = reinterpret_cast<int*>(ws + L.empty_rows);
+  int* merge_cnt = reinterpret_cast<int*>(ws + L.merge_cnt);
+  const int ppg = pairs_per_group;
+  int* s_lo = s_dyn;
+  int* s_rank = s_dyn + (ppg + 1);
+  const bool rows_in_smem = batch <= kPlanSmemRows;
+  int* r_ts = rows_in_smem ? s_dyn + 2 * (ppg + 1) : tile_start;
+  int* r_cost = rows_in_smem ? r_ts + (batch + 1) : reinterpret_cast<int*>(ws + L.row_cost);
 
   const int tid = threadIdx.x;
   // the attention kernel may begin its prologue now; it reads the plan only
   // after this grid has completed (griddepcontrol.wait)
   ptx::grid_dep_launch();
+  for (int i = tid; i < 2 * L.max_slots; i += blockDim.x) merge_cnt[i] = 0;
   const int per = (batch + blockDim.x - 1) / blockDim.x;
   const int lo = min(batch, tid * per), hi = min(batch, lo + per);
   const int max_len = max_pages * kPage;
 
   // pass 1: clamp lengths, tiles per row, prefix sums
-  int local = 0;
+  int local = 0, local_ne = 0;
   for (int b = lo; b < hi; ++b) {
     int s = seq_lens[b];
     if (s < 0 || s > max_len) {
@@ -87,122 +110,156 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
     lens[b] = s;
     local += (s + kPage - 1) / kPage;
+    local_ne += s > 0 ? 1 : 0;
   }
   int total = 0;
   int excl = block_exclusive_scan(local, s_warp, &total);
-  for (int b = lo; b < hi; ++b) {
-    tile_start[b] = excl;
-    excl += (lens[b] + kPage - 1) / kPage;
-  }
   // Row costs for the partition: a row with pages costs its pages plus
   // kSegCost pages' worth for its segment start (query load, output write,
   // pipeline refill).
-  int local_ne = 0;
-  for (int b = lo; b < hi; ++b) local_ne += lens[b] > 0 ? 1 : 0;
   int ne_total = 0;
   int ne_excl = block_exclusive_scan(local_ne, s_warp, &ne_total);
   for (int b = lo; b < hi; ++b) {
-    row_cost[b] = tile_start[b] + kSegCost * ne_excl;
-    ne_excl += lens[b] > 0 ? 1 : 0;
+    const int n = (lens[b] + kPage - 1) / kPage;
+    r_ts[b] = excl;
+    if (rows_in_smem) tile_start[b] = excl;
+    r_cost[b] = excl + kSegCost * ne_excl;
+    excl += n;
+    ne_excl += n > 0 ? 1 : 0;
   }
   if (tid == 0) {
+    r_ts[batch] = total;
     tile_start[batch] = total;
-    row_cost[batch] = total + kSegCost * ne_total;
-    s_chunk = total > 0 ? (total + pairs_per_group - 1) / pairs_per_group : 1;
+    r_cost[batch] = total + kSegCost * ne_total;
+    s_chunk = total > 0 ? (total + ppg - 1) / ppg : 1;
   }
   __syncthreads();
   const int chunk = s_chunk;
 
   // Pair p starts where the cumulative cost reaches p/ppg of the total: in
   // the row whose cost range holds that point, past the row's start cost.
+  // pair_b0[p]: the row holding the pair's first page (the last row whose
+  // pages start at or before it), where the attention kernel begins walking.
   const long long cost_total = static_cast<long long>(total) + static_cast<long long>(kSegCost) * ne_total;
-  for (int pp = tid; pp <= pairs_per_group; pp += blockDim.x) {
+  for (int pp = tid; pp <= ppg; pp += blockDim.x) {
     int x = pp == 0 ? 0 : total;
-    if (pp > 0 && pp < pairs_per_group) {
-      const long long target = cost_total * pp / pairs_per_group;
+    if (pp > 0 && pp < ppg) {
+      const long long target = cost_total * pp / ppg;
       int l = 0, r = batch - 1;            // largest row with row_cost <= target
       while (l < r) {
         const int mid = (l + r + 1) >> 1;
-        if (row_cost[mid] <= target) l = mid; else r = mid - 1;
+        if (r_cost[mid] <= target) l = mid; else r = mid - 1;
       }
-      const int n = tile_start[l + 1] - tile_start[l];
-      const long long off = target - row_cost[l] - (n > 0 ? kSegCost : 0);
-      x = tile_start[l] + static_cast<int>(off < 0 ? 0 : (off > n ? n : off));
+      const int n = r_ts[l + 1] - r_ts[l];
+      const long long off = target - r_cost[l] - (n > 0 ? kSegCost : 0);
+      x = r_ts[l] + static_cast<int>(off < 0 ? 0 : (off > n ? n : off));
     }
+    s_lo[pp] = x;
     pair_lo[pp] = x;
+    if (pp < ppg) {
+      int l = 0, r = batch - 1;            // largest row with tile_start <= x
+      while (l < r) {
+        const int mid = (l + r + 1) >> 1;
+        if (r_ts[mid] <= x) l = mid; else r = mid - 1;
+      }
+      pair_b0[pp] = l;
+    }
   }
   __syncthreads();
+  // pair_bl[p]: the row holding the pair's last page (where the pair ends,
+  // and whose split merge it may take part in); -1 for an empty range.
+  for (int pp = tid; pp < ppg; pp += blockDim.x) {
+    const int x = s_lo[pp + 1] - 1;
+    int l = -1;
+    if (x >= s_lo[pp]) {
+      int r = batch - 1;
+      l = 0;
+      while (l < r) {
+        const int mid = (l + r + 1) >> 1;
+        if (r_ts[mid] <= x) l = mid; else r = mid - 1;
+      }
+    }
+    pair_bl[pp] = l;
+  }
   // pair_rank[p]: pairs before p that have pages.  A pair range can be empty
   // (its cost share falls inside a row's start cost); a split row's parts
   // are the non-empty pairs over it, numbered by rank.
   if (tid < 32) {
     int carry = 0;
-    for (int base = 0; base <= pairs_per_group; base += 32) {
+    for (int base = 0; base <= ppg; base += 32) {
       const int pp = base + tid;
-      const int ne = pp < pairs_per_group && pair_lo[pp + 1] > pair_lo[pp] ? 1 : 0;
+      const int ne = pp < ppg && s_lo[pp + 1] > s_lo[pp] ? 1 : 0;
       int x = ne;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (tid >= o) x += y;
       }
-      if (pp <= pairs_per_group) pair_rank[pp] = carry + x - ne;
+      if (pp <= ppg) {
+        s_rank[pp] = carry + x - ne;
+        pair_rank[pp] = carry + x - ne;
+      }
       carry += __shfl_sync(0xffffffffu, x, 31);
     }
   }
   __syncthreads();
   // the pair whose page range [pair_lo[p], pair_lo[p+1]) holds page t
   auto pair_of = [&](int t) {
-    int l = 0, r = pairs_per_group - 1;
+    int l = 0, r = ppg - 1;
     while (l < r) {
       const int mid = (l + r + 1) >> 1;
-      if (pair_lo[mid] <= t) l = mid; else r = mid - 1;
+      if (s_lo[mid] <= t) l = mid; else r = mid - 1;
     }
     return l;
   };
 
   // pass 2: pairs covering each row; slots for rows that are split
   local = 0;
-  int local_comb = 0;
+  int local_empty = 0;
   for (int b = lo; b < hi; ++b) {
     const int n = (lens[b] + kPage - 1) / kPage;
     int parts = 0, fp = 0;
     if (n > 0) {
-      fp = pair_of(tile_start[b]);
-      parts = pair_rank[pair_of(tile_start[b] + n - 1) + 1] - pair_rank[fp];
+      const int t0 = r_ts[b];
+      fp = pair_of(t0);
+      parts = s_rank[pair_of(t0 + n - 1) + 1] - s_rank[fp];
     }
     first_pair[b] = fp;
+    n_parts[b] = parts;
     local += parts > 1 ? parts : 0;
-    local_comb += (parts != 1) ? 1 : 0;
+    local_empty += parts == 0 ? 1 : 0;
   }
   int slots_total = 0;
   int slot_excl = block_exclusive_scan(local, s_warp, &slots_total);
-  int comb_total = 0;
-  int comb_excl = block_exclusive_scan(local_comb, s_warp, &comb_total);
+  int empty_total = 0;
+  int empty_excl = block_exclusive_scan(local_empty, s_warp, &empty_total);
   for (int b = lo; b < hi; ++b) {
-    const int n = (lens[b] + kPage - 1) / kPage;
-    int parts = 0;
-    if (n > 0) parts = pair_rank[pair_of(tile_start[b] + n - 1) + 1] - pair_rank[first_pair[b]];
+    const int parts = n_parts[b];
     slot_base[b] = parts > 1 ? slot_excl : -1;
-    if (parts != 1) {
-      for (int i = 0; i < sq; ++i) {
-        const int k = comb_excl * sq + i;
-        comb_row[k] = b * sq + i;
-        comb_start[k] = parts > 1 ? i * slots_total + slot_excl : 0;
-        comb_count[k] = parts > 1 ? parts : 0;
-      }
-      ++comb_excl;
-    }
     if (parts > 1) slot_excl += parts;
+    if (parts == 0) empty_rows[empty_excl++] = b;
   }
   if (tid == 0) {
     hdr->n_tiles = total;
     hdr->chunk = chunk;
     hdr->slots_per_query = slots_total;
-    hdr->n_comb = comb_total * sq;
-    hdr->pairs_per_group = pairs_per_group;
+    hdr->n_empty = empty_total;
+    hdr->pairs_per_group = ppg;
     hdr->abort_flag = 0;
     hdr->fp8_range = 0;
+  }
+  // Rows with no token: out = 0, lse = -inf for every query index (the
+  // attention kernel has no page of theirs to visit).
+  __syncthreads();
+  constexpr int kRowVec = kHeads * kDc * 2 / 16;   // 16-byte stores per output row
+  for (int k = 0; k < empty_total; ++k) {
+    const int b = empty_rows[k];
+    for (int i = 0; i < sq; ++i) {
+      const size_t row = static_cast<size_t>(b) * sq + i;
+      uint4* dst = reinterpret_cast<uint4*>(out + row * kHeads * kDc);
+      for (int e = tid; e < kRowVec; e += blockDim.x) dst[e] = make_uint4(0, 0, 0, 0);
+      if (tid < kHeads) lse[row * kHeads + tid] = -INFINITY;
+    }
   }
 }
 
@@ -236,15 +293,16 @@ __global__ void __launch_bounds__(256) sparse_prep_kernel(const int32_t* __restr
 cudaError_t launch_sparse_prep(const int32_t* token_slots, int rows, int topk, int num_slots, void* ws,
                                const WsLayout& L, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  sparse_prep_kernel<<<rows, 256, 0, stream>>>(token_slots, topk, num_slots, static_cast<uint8_t*>(ws), L);
-  return cudaGetLastError();
+  return launch_kernel(sparse_prep_kernel, dim3(rows), dim3(256), 0, stream, token_slots, topk, num_slots,
+                       static_cast<uint8_t*>(ws), L);
 }
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_pages, int pairs_per_group,
-                        void* ws, const WsLayout& L, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, batch, sq, max_pages, pairs_per_group,
-                                      static_cast<uint8_t*>(ws), L);
-  return cudaGetLastError();
+                        void* ws, const WsLayout& L, __nv_bfloat16* out, float* lse, cudaStream_t stream) {
+  const size_t smem = sizeof(int) * (2 * static_cast<size_t>(pairs_per_group + 1) +
+                                     (batch <= kPlanSmemRows ? 2 * static_cast<size_t>(batch + 1) : 0));
+  return launch_kernel(plan_kernel, dim3(1), dim3(1024), smem, stream, seq_lens, batch, sq, max_pages,
+                       pairs_per_group, static_cast<uint8_t*>(ws), L, out, lse);
 }
 
 }  // namespace mla

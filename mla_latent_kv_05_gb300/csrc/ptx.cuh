@@ -59,6 +59,24 @@ __device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t* v) {
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
                : "l"(p));
 }
+// 32-byte global load through L2 only (address 32-byte aligned), for data
+// that other CTAs wrote during this kernel.
+__device__ __forceinline__ void ld_global_cg_v8(const void* p, uint32_t* v) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p) : "memory");
+}
+// Load with acquire semantics at GPU scope.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Add with release semantics at GPU scope (prior writes are visible to a
+// thread that acquires the new value).
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
 // 32-byte global store (address 32-byte aligned): one whole sector per lane.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
@@ -141,16 +159,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
                " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
                :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy) : "memory");
 }
-// Same, multicast: the box lands at offset `dst` of the shared memory of every
-// CTA in `mask` (this CTA need not be one of them), and each of them gets the
-// complete_tx on its barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const void* tmap, uint32_t bar, int32_t x, int32_t y,
-                                               int32_t z, int32_t w, uint16_t mask, uint64_t policy) {
-  asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-               ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;"
-               :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask), "l"(policy)
-               : "memory");
-}
 // 1-D bulk copy global -> shared (size and both addresses multiples of 16 B).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                           uint64_t policy) {
@@ -167,6 +175,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
 // the barrier's expected count includes this arrival (no increment).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+// Wait until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 // Prefetch a contiguous global range (16-byte aligned, multiple of 16 B) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {

@@ -170,10 +170,8 @@ cudaError_t launch_wuv(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* o, 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  wuv_kernel<<<dim3(kHeads, (rows + 127) / 128), 128, kSmem, stream>>>(tm_o, tm_w, rows,
-                                                                        static_cast<__nv_bfloat16*>(out),
-                                                                        static_cast<PlanHeader*>(hdr));
-  return cudaGetLastError();
+  return launch_kernel(wuv_kernel, dim3(kHeads, (rows + 127) / 128), dim3(128), kSmem, stream, tm_o, tm_w, rows,
+                       static_cast<__nv_bfloat16*>(out), static_cast<PlanHeader*>(hdr));
 }
 
 }  // namespace mla

@@ -36,3 +36,32 @@ def test_reference_arm_prints_the_contract_line(workload):
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     kv = {"1": "bf16", "7": "fp4"}[workload]
     assert d["config"]["kv_dtype"] == kv
+
+
+def test_gpus_flag_must_match_the_launchers_world_size():
+    # --gpus 2 without a launcher that starts two ranks is an error, not a
+    # silent one-GPU run
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--workload", "1",
+                        "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env={k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")})
+    assert r.returncode != 0
+    assert "WORLD_SIZE=1" in r.stderr
+
+
+def test_two_ranks_through_torchrun_print_one_line():
+    # the launcher the N>1 contract names (gloo on this CPU host): two ranks
+    # start, rank 0 alone prints, both exit 0
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+                        "--gpus", "2", "--workload", "1", "--steps", "3", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["impl"] == "reference"

@@ -69,6 +69,7 @@ def test_workload1_oracle_sized(cuda_device):
 
 @pytest.mark.parametrize("lens", [
     [1, 2, 63, 64, 65, 127, 128, 129],
+    [95, 96, 97, 191, 192, 193, 288],   # the 96-token score-tile edges
     [1000, 4097, 3, 700],
     [5000],
 ])
@@ -89,6 +90,25 @@ def test_multi_token_causal(cuda_device, sq, lens):
 
 def test_empty_rows(cuda_device):
     inp = gen.make_inputs(4, 1, [0, 70, 0, 1], seed=3, physical_pages=4)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+def test_empty_rows_with_multi_token_queries(cuda_device):
+    # rows with no token are written by the planner for every query index;
+    # a one-token row leaves its first query with nothing to see
+    inp = gen.make_inputs(3, 2, [0, 1, 130], seed=4)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
+@pytest.mark.parametrize("sq,lens", [(1, [20000]), (2, [9000, 40])])
+def test_rows_split_over_many_pairs(cuda_device, sq, lens):
+    # one long row cut into dozens of parts: the part that finishes last
+    # merges all the others' partials with its own output
+    inp = gen.make_inputs(len(lens), sq, lens, seed=31 + sq)
     out, lse, st = run_gpu(inp)
     assert st == 0
     assert_close(out, lse, *oracle(inp))

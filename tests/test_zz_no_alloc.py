@@ -1,12 +1,15 @@
 """mla_decode_bf16_noalloc (the decode on the library's own static scratch)
-against mla_decode_bf16 with a caller workspace, through the C ABI.
+against mla_decode_bf16 with a caller workspace, through the C ABI, and
+against the float64 oracle.
 
 Two calls in a row on different problems (a ragged batch whose rows are split
 over many CTA pairs, then causal two-token queries), each compared with the
-workspace entry point on the same inputs within the parity tolerance
-(max|dout| <= 1e-2 * max|ref|, max|dlse| <= 1e-3).  The device's free memory
-must not move across the calls once the first call has done its set-up.
-Collected last so that it also runs after every other GPU test.
+workspace entry point and with the oracle on the same inputs within the
+parity tolerance (max|dout| <= 1e-2 * max|ref|, max|dlse| <= 1e-3).  Neither
+torch's allocator statistics nor the device's free memory may move across
+the calls once the first call has done its set-up (the free-memory reading
+is retaken once if another process on the device moved it).  Collected last
+so that it also runs after every other GPU test.
 """
 import ctypes
 
@@ -16,6 +19,7 @@ import torch
 
 from mla_latent_kv_05_gb300 import binding
 from mla_latent_kv_05_gb300 import inputs as gen
+from oracle import mla_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +36,13 @@ def _problems():
 def _device(inp):
     return (inp.q_absorbed.cuda(), inp.q_rope.cuda(), inp.kv_cache.cuda(), inp.block_table.cuda(),
             inp.seq_lens.cuda())
+
+
+def _oracle(inp):
+    rows = mla_oracle.cache_rows(inp.kv_cache.double().numpy(), "bf16")
+    o, l_ = mla_oracle.mla_decode(inp.q_absorbed.double().numpy(), inp.q_rope.double().numpy(), rows,
+                                  inp.block_table.numpy(), inp.seq_lens.numpy(), inp.scale)
+    return torch.from_numpy(o), torch.from_numpy(l_)
 
 
 def _compare(out, lse, ref_out, ref_lse):
@@ -66,21 +77,30 @@ def test_noalloc_matches_workspace_entry_on_consecutive_calls(cuda_device):
     assert int(status[0].item()) == 0
     _compare(*outs[0], *refs[0])
 
-    for o in outs:
-        o[0].fill_(7)
-        o[1].fill_(7)
-    for s in status:
-        s.fill_(-99)
-    torch.cuda.synchronize()
-    free_before = torch.cuda.mem_get_info()[0]
-    for p, d, o, s in zip(probs, dev, outs, status):
-        binding.mla_decode_bf16_noalloc(*d, p.scale, out=o[0], lse=o[1], device_status=s)
-    torch.cuda.synchronize()
-    free_after = torch.cuda.mem_get_info()[0]
-    assert free_after == free_before
-    for o, r, s in zip(outs, refs, status):
+    oracles = [_oracle(p) for p in probs]
+
+    def run_both():
+        for o in outs:
+            o[0].fill_(7)
+            o[1].fill_(7)
+        for s in status:
+            s.fill_(-99)
+        torch.cuda.synchronize()
+        stats = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved())
+        free_before = torch.cuda.mem_get_info()[0]
+        for p, d, o, s in zip(probs, dev, outs, status):
+            binding.mla_decode_bf16_noalloc(*d, p.scale, out=o[0], lse=o[1], device_status=s)
+        torch.cuda.synchronize()
+        assert (torch.cuda.memory_allocated(), torch.cuda.memory_reserved()) == stats
+        return torch.cuda.mem_get_info()[0] - free_before
+
+    if run_both() != 0:
+        # another process may have moved the device's free memory: measure once more
+        assert run_both() == 0
+    for o, r, orc, s in zip(outs, refs, oracles, status):
         assert int(s.item()) == 0
         _compare(*o, *r)
+        _compare(*o, *orc)
 
 
 def test_noalloc_rejects_rows_beyond_its_scratch(cuda_device):
