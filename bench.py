@@ -1,7 +1,7 @@
 """Benchmark: MLA decode over a paged latent KV cache on GB300.
 
 One step = one full decode call through the C ABI (split-KV planner, paired
-tcgen05 attention kernel that also merges its split rows) over one batch of
+tcgen05 attention kernel, LSE merge of the split rows) over one batch of
 synthetic inputs that are already resident in HBM.  Default workload: batch 64, Sq 1, seq_lens
 drawn uniformly in [1, 32768] (seed 1003), bf16 cache with shuffled pages.
 
@@ -320,13 +320,12 @@ def run_ours(args):
     lse = torch.empty((inp.batch, inp.sq, 128), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     if sp is not None:
-        # sparse top-k decode: three launches per call (compaction, planner,
-        # attention with the split merge); the per-step inputs are q, q_rope
-        # and the lists
+        # sparse top-k decode: four launches per call (compaction, planner,
+        # attention, merge); the per-step inputs are q, q_rope and the lists
         counts = gen.sparse_counts(sp)
         slots = sp.token_slots.to(dev)
         ws = binding.alloc_workspace_sparse(inp.batch, inp.sq, sp.topk, dev)
-        launches = 3
+        launches = 4
         uploads = [(sp.token_slots.pin_memory(), slots)]
 
         def call(qb, qrb, extra, outb, lseb):
@@ -341,10 +340,9 @@ def run_ours(args):
         bt = inp.block_table.to(dev)
         sl = inp.seq_lens.to(dev)
         ws = binding.alloc_workspace(inp.batch, inp.sq, dev)
-        # planner, attention with the split merge (FP8, FP4: the exact pass
-        # after the f16 pass is a third launch, which returns at once unless
-        # needed)
-        launches = 2 if inp.kv_dtype == "bf16" else 3
+        # planner, attention, merge (FP8, FP4: the exact pass after the f16
+        # pass is a fourth launch, which returns at once unless needed)
+        launches = 3 if inp.kv_dtype == "bf16" else 4
         uploads = [(inp.block_table.pin_memory(), bt), (inp.seq_lens.pin_memory(), sl)]
 
         def call(qb, qrb, extra, outb, lseb):

@@ -79,10 +79,9 @@ typedef enum {
 int mla_workspace_size(int batch, int sq, int num_heads, int page_size, size_t* bytes);
 
 /* MLA decode over a bf16 latent cache (guide section 1.1; see top of file).
- * Queues two kernels: the split-KV planner, and the paired tcgen05 decode
- * kernel, which also merges the parts of the rows it split (the part that
- * finishes last combines them by the rule of mla_combine_splits).
- * workspace: device memory of at least
+ * Queues three kernels: the split-KV planner, the paired tcgen05 decode
+ * kernel, and the merge of the rows it split (the rule of
+ * mla_combine_splits).  workspace: device memory of at least
  * mla_workspace_size(...) bytes, 256-byte aligned, not shared with a call
  * that may run concurrently.  Returns MLA_OK or a negative mla_status. */
 int mla_decode_bf16(const uint16_t* q_absorbed, const uint16_t* q_rope,

@@ -1,6 +1,6 @@
 // C ABI of the MLA decode library: argument validation, workspace sizing,
 // tensor-map creation and the launch sequence (planner -> paired decode
-// kernel, which also merges the split rows), all on the caller's stream.
+// kernel -> split merge), all on the caller's stream.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -123,10 +123,11 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   p.lse = lse;
   p.ws = static_cast<uint8_t*>(workspace);
   p.L = L;
-  // The attention kernel is a programmatic dependent of the planner, so its
-  // prologue overlaps the planner.  A call with the profiling hook set
-  // records its events around the attention kernel and launches it without
-  // that overlap, so that the events bracket it alone.
+  // The three kernels are chained with programmatic dependent launch, so the
+  // attention kernel's prologue overlaps the planner and the merge kernel's
+  // launch overlaps the attention kernel's tail.  A call with the profiling
+  // hook set records its events around the attention kernel and launches the
+  // kernels without that overlap, so that the events bracket it alone.
   cudaEvent_t ev0 = g_prof_before, ev1 = g_prof_after;
   g_prof_before = g_prof_after = nullptr;
   const bool pdl = ev0 == nullptr;
@@ -137,6 +138,7 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   else le = launch_decode_bf16(maps, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine_plan(workspace, L, batch, sq, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -176,7 +178,7 @@ int static_scratch(void** ptr) {
 constexpr int kMaxTopk = 16384;
 
 // Sparse top-k decode: compact the slot lists, plan the B*Sq query rows as a
-// batch of rows with one query each, gather-attend (merging split rows).
+// batch of rows with one query each, gather-attend, merge.
 int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache, const int32_t* token_slots,
                int batch, int sq, int topk, int num_heads, int num_pages, int page_size, float softmax_scale,
                uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream_ptr) {
@@ -227,6 +229,7 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_decode_sparse(p, pairs, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine_plan(workspace, L, rows, 1, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 

@@ -1,10 +1,9 @@
-// Split-KV merge of caller-made parts (the public mla_combine_splits; the
-// decode calls merge their own splits inside the attention kernel).
-// Attention over disjoint token sets combines exactly from each part's
-// normalised output and LSE:
+// Split-KV merge.  Attention over disjoint token sets combines exactly from
+// each part's normalised output and LSE:
 //     L = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - L) * out_s.
-// One warp per (output row, head), 16 values per lane, fp32 partials in,
-// bf16 out.
+// Two kernels: the decode calls' merge of their own split rows (bf16
+// partials, from the plan), and the public mla_combine_splits (fp32
+// partials, caller's indptr).  One warp per (output row, head), bf16 out.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -89,7 +88,94 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (lane == 0) lse[static_cast<size_t>(row) * kHeads + h] = sum > 0.f ? L + logf(sum) : -INFINITY;
 }
 
+// The decode's split rows, launched as a programmatic dependent of the
+// attention kernel (its partials are read only after that grid completed):
+// grid (B*Sq, 128/8), one warp per (row, head), lane = 16 latent columns
+// (one 32-byte sector).  Row k = b*Sq + i merges its bf16 partials at slots
+// [i*spq + slot_base[b], + n_parts[b]) when the planner split it
+// (n_parts[b] > 1); other rows were written by the attention kernel (one
+// part) or the planner (no token).  Four parts' loads are in flight at a
+// time; the parts are summed in slot order.
+__global__ void __launch_bounds__(256) combine_plan_kernel(const uint8_t* __restrict__ ws, WsLayout Lw, int sq,
+                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  ptx::grid_dep_wait();
+  const int k = blockIdx.x;
+  const int b = k / sq, i = k - b * sq;
+  const int parts = reinterpret_cast<const int*>(ws + Lw.n_parts)[b];
+  if (parts <= 1) return;
+  const int spq = reinterpret_cast<const PlanHeader*>(ws)->slots_per_query;
+  const int start = i * spq + reinterpret_cast<const int*>(ws + Lw.slot_base)[b];
+  const float* part_lse = reinterpret_cast<const float*>(ws + Lw.part_lse);
+  const __nv_bfloat16* part_out = reinterpret_cast<const __nv_bfloat16*>(ws + Lw.part_out);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
+  float L = -INFINITY;
+  for (int s = lane; s < parts; s += 32) L = fmaxf(L, part_lse[static_cast<size_t>(start + s) * kHeads + h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  float sum = 0.f;
+  if (L != -INFINITY) {
+    for (int s0 = 0; s0 < parts; s0 += 32) {
+      const int sl = s0 + lane;
+      const float v = sl < parts ? part_lse[static_cast<size_t>(start + sl) * kHeads + h] : -INFINITY;
+      const float wl = v == -INFINITY ? 0.f : __expf(v - L);
+      const int n = min(32, parts - s0);
+      for (int j0 = 0; j0 < n; j0 += 4) {
+        uint32_t x[4][8];
+        float wgt[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wgt[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
+          if (j0 + u < n) {
+            ptx::ld_global_cg_v8(part_out + (static_cast<size_t>(start + s0 + j0 + u) * kHeads + h) * kDc + 16 * lane, x[u]);
+          } else {
+            wgt[u] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[u][e] = 0u;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          sum += wgt[u];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[u][e]));
+            acc[2 * e] = fmaf(wgt[u], f.x, acc[2 * e]);
+            acc[2 * e + 1] = fmaf(wgt[u], f.y, acc[2 * e + 1]);
+          }
+        }
+      }
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  uint32_t o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    __nv_bfloat162 bb = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    o[e] = *reinterpret_cast<uint32_t*>(&bb);
+  }
+  ptx::st_global_v8(out + (static_cast<size_t>(k) * kHeads + h) * kDc + 16 * lane, o);
+  if (lane == 0) lse[static_cast<size_t>(k) * kHeads + h] = sum > 0.f ? L + logf(sum) : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int batch, int sq, __nv_bfloat16* out, float* lse,
+                                bool pdl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch * sq, kHeads / 8, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_plan_kernel, static_cast<const uint8_t*>(ws), Lw, sq, out, lse);
+}
 
 // Public merge: parts of row r are [indptr[r], indptr[r+1]).
 cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,

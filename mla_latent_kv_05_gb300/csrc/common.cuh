@@ -37,8 +37,7 @@ struct PlanHeader {
 
 // Offsets (bytes) of the plan arrays and split partials inside the workspace.
 struct WsLayout {
-  size_t lens, tile_start, row_cost, pair_lo, pair_rank, pair_b0, pair_bl, first_pair, slot_base, n_parts,
-      empty_rows, merge_cnt;
+  size_t lens, tile_start, row_cost, pair_lo, pair_rank, pair_b0, first_pair, slot_base, n_parts, empty_rows;
   size_t part_lse, part_out;
   size_t sp_lens, sp_slots;   // sparse decode: listed tokens per row, compacted slot lists [rows, topk]
   size_t total;
@@ -61,14 +60,10 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int sq, int pairs, int 
   L.pair_lo = o;     o = align256(o + sizeof(int) * (pg + 1));
   L.pair_rank = o;   o = align256(o + sizeof(int) * (pg + 1));
   L.pair_b0 = o;     o = align256(o + sizeof(int) * (pg + 1));
-  L.pair_bl = o;     o = align256(o + sizeof(int) * (pg + 1));
   L.first_pair = o;  o = align256(o + sizeof(int) * batch);
   L.slot_base = o;   o = align256(o + sizeof(int) * batch);
   L.n_parts = o;     o = align256(o + sizeof(int) * batch);
   L.empty_rows = o;  o = align256(o + sizeof(int) * batch);
-  // merge counters: two passes (the FP8/FP4 exact pass has its own) x split
-  // rows (indexed by their first partial slot)
-  L.merge_cnt = o;   o = align256(o + sizeof(int) * 2 * static_cast<size_t>(L.max_slots));
   L.part_lse = o;    o = align256(o + sizeof(float) * static_cast<size_t>(L.max_slots) * kHeads);
   L.part_out = o;    o = align256(o + 2 * static_cast<size_t>(L.max_slots) * kHeads * kDc);   // bf16 partials
   L.sp_lens = o;     o = align256(o + (topk > 0 ? sizeof(int) * batch : 0));

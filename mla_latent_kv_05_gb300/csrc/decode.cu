@@ -214,6 +214,7 @@ struct SegWalker {
       const int a = __ldg(tile_start + b), e = __ldg(tile_start + b + 1);
       if (a >= hi) { b = batch; return false; }
       const int cb = b++;
+      if (e >= hi) b = batch;   // this segment reaches the end of the range: no read for the next call
       if (e > a) {
         s.b = cb;
         s.t0 = max(lo, a) - a;
@@ -471,150 +472,6 @@ __device__ __forceinline__ void load_q_rolled(const uint8_t* qa, const uint8_t* 
   }
 }
 
-// ------------------------------------------------------------ split-row merge
-// A row cut into P > 1 parts is merged inside the attention kernel.  Every
-// part writes its normalised bf16 partial (rank 0's epilogue warps) and its
-// lse (rank 1's first softmax group), and each of those warps then adds one
-// to the row's counter with a release.  Parts 0 .. P-2 of a row always end
-// their pair's page range (the row goes on into the next pair), so they run
-// last in their pairs; after their own part they merge a slice of the 128
-// heads each (both SMs of the pair, one warp per head), once the counter
-// shows every part written; every warp of both CTAs joins in (a merger's
-// roles are all done by then).  Part P-1 never waits, and no part waits for
-// a merger, so every wait ends.  The parts are summed in slot order, so the
-// result does not depend on which part finishes first.
-// The warp's writes (and those it has acquired) are visible GPU-wide before
-// the row's counter moves.
-__device__ __forceinline__ void count_written(uint32_t* cnt, int lane) {
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) ptx::red_release_gpu_add(cnt, 1u);
-}
-
-// Wait (warp-uniformly, bounded) until the counter reaches `want`.
-__device__ __forceinline__ bool wait_count(const uint32_t* cnt, uint32_t want, PlanHeader* hdr) {
-  if (__all_sync(0xffffffffu, ptx::ld_acquire_gpu(cnt) >= want)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t n = 1;; ++n) {
-    __nanosleep(128);   // the warps of this SM that still work get the issue slots
-    if (__all_sync(0xffffffffu, ptx::ld_acquire_gpu(cnt) >= want)) return true;
-    if ((n & 63u) == 0) {
-      bool give_up = read_status(&hdr->abort_flag) != 0;
-      if (!give_up && ptx::globaltimer() - t0 > MLA_WAIT_TIMEOUT_NS) {
-        set_status(&hdr->status, MLA_STATUS_TIMEOUT);
-        atomicExch(&hdr->abort_flag, 1);
-        give_up = true;
-      }
-      if (__any_sync(0xffffffffu, give_up)) return false;
-    }
-  }
-}
-
-// Merge heads [h_begin, h_end) of a split row from its `parts` partials at
-// slots slot0 ..: warp g of nw takes heads h_begin + g, + nw, ..., kHB at a
-// time so that their loads are in flight together; lane = 16 latent columns
-// (one 32-byte sector of a partial row).  L = max lse, weights exp(lse - L),
-// out = sum_s w_s o_s / sum_s w_s, lse = L + ln sum_s w_s.
-// kHB heads per round (more in flight, more registers).
-template <int kHB>
-__device__ __forceinline__ void merge_heads(const __nv_bfloat16* part_out, const float* part_lse, int slot0, int parts,
-                                         int h_begin, int h_end, int g, int nw, int lane, __nv_bfloat16* out_row,
-                                         float* lse_row) {
-  auto lse_at = [&](int s, int h) { return __ldcg(part_lse + static_cast<size_t>(slot0 + s) * kHeads + h); };
-  auto row_at = [&](int s, int h) {
-    return part_out + (static_cast<size_t>(slot0 + s) * kHeads + h) * kDc + 16 * lane;
-  };
-#pragma unroll 1
-  for (int h0 = h_begin + g; h0 < h_end; h0 += kHB * nw) {
-    int hh[kHB];
-    bool on[kHB];
-#pragma unroll
-    for (int j = 0; j < kHB; ++j) {
-      hh[j] = h0 + j * nw;
-      on[j] = hh[j] < h_end;
-    }
-    // Issued together: every lane's first lse (part `lane`) and the first
-    // two parts' values, so that a two-part row takes one round trip.
-    float v0[kHB];
-    uint32_t x[2][kHB][8];
-#pragma unroll
-    for (int j = 0; j < kHB; ++j) {
-      v0[j] = (lane < parts && on[j]) ? lse_at(lane, hh[j]) : -INFINITY;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (t < parts && on[j]) {
-          ptx::ld_global_cg_v8(row_at(t, hh[j]), x[t][j]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[t][j][e] = 0u;
-        }
-      }
-    }
-    float L[kHB], sum[kHB], acc[kHB][16];
-#pragma unroll
-    for (int j = 0; j < kHB; ++j) {
-      L[j] = v0[j];
-      for (int s = lane + 32; s < parts; s += 32)
-        if (on[j]) L[j] = fmaxf(L[j], lse_at(s, hh[j]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L[j] = fmaxf(L[j], __shfl_xor_sync(0xffffffffu, L[j], o));
-      sum[j] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[j][e] = 0.f;
-    }
-    for (int s0 = 0; s0 < parts; s0 += 32) {
-      // lane u: the weight of part s0 + u
-      float wl[kHB];
-#pragma unroll
-      for (int j = 0; j < kHB; ++j) {
-        const float v = s0 == 0 ? v0[j] : ((s0 + lane < parts && on[j]) ? lse_at(s0 + lane, hh[j]) : -INFINITY);
-        wl[j] = v == -INFINITY ? 0.f : __expf(v - L[j]);
-      }
-      const int n = min(32, parts - s0);
-      for (int u = 0; u < n; u += 2) {
-        if (s0 + u > 0) {
-#pragma unroll
-          for (int j = 0; j < kHB; ++j) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (u + t < n && on[j]) {
-                ptx::ld_global_cg_v8(row_at(s0 + u + t, hh[j]), x[t][j]);
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[t][j][e] = 0u;
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-#pragma unroll
-          for (int j = 0; j < kHB; ++j) {
-            const float w = u + t < n && on[j] ? __shfl_sync(0xffffffffu, wl[j], u + t) : 0.f;
-            sum[j] += w;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[t][j][e]));
-              acc[j][2 * e] = fmaf(w, f.x, acc[j][2 * e]);
-              acc[j][2 * e + 1] = fmaf(w, f.y, acc[j][2 * e + 1]);
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kHB; ++j) {
-      if (!on[j]) continue;
-      const float inv = sum[j] > 0.f ? 1.f / sum[j] : 0.f;
-      uint32_t o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = pack_bf16x2(acc[j][2 * e] * inv, acc[j][2 * e + 1] * inv);
-      ptx::st_global_v8(out_row + static_cast<size_t>(hh[j]) * kDc + 16 * lane, o);
-      if (lane == 0) lse_row[hh[j]] = sum[j] > 0.f ? L[j] + logf(sum[j]) : -INFINITY;
-    }
-  }
-}
-
 }  // namespace dk
 
 // kMode 0: bf16 cache via TMA; 1: FP8 cache via bulk copies + dequant to
@@ -660,7 +517,6 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
   float* part_lse = reinterpret_cast<float*>(p.ws + p.L.part_lse);
   __nv_bfloat16* part_out = reinterpret_cast<__nv_bfloat16*>(p.ws + p.L.part_out);
   const int* n_parts = reinterpret_cast<const int*>(p.ws + p.L.n_parts);
-  uint32_t* merge_cnt = reinterpret_cast<uint32_t*>(p.ws + p.L.merge_cnt);
   auto BAR = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
   // physical page of row-local half page hp of batch row b (or -1 if out of range)
   auto half_page = [&](int b, int hp) -> int {
@@ -736,6 +592,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
   const int* pair_rank = reinterpret_cast<const int*>(p.ws + p.L.pair_rank);   // non-empty pairs before p
   const int lo = pair_lo[pl], hi = pair_lo[pl + 1];     // this pair's page range (cost-balanced by the planner)
   const int b0 = reinterpret_cast<const int*>(p.ws + p.L.pair_b0)[pl];   // the row holding page lo
+
   const int sq = p.sq;
   // the exact FP8 pass after an f16 pass runs only if that pass flagged an
   // input outside the f16-exact range
@@ -1378,8 +1235,6 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
         const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;   // correctly rounded, as 1/l
         if (split) {
           part_lse[static_cast<size_t>(slot) * kHeads + h] = lse_v;
-          count_written(merge_cnt + static_cast<size_t>(p.fp8_fallback) * p.L.max_slots + group * spq + slot_base[sg.b],
-                        lane);
         } else {
           p.lse[static_cast<size_t>(row) * kHeads + h] = lse_v;
         }
@@ -1468,50 +1323,39 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
       ptx::tc_fence_after();
       if (!wait_warp<true>(BAR(MBFULL + ms), mphase, hdr)) { ok = false; break; }
       const float inv_l = mail[ms * 128 + h];
-      // out = bf16(O / l): into the output row, or (split rows) into the
-      // row's partial slot, counted written afterwards (the merge below)
       const int parts = n_parts[sg.b];
       const int slot0 = parts > 1 ? group * spq + slot_base[sg.b] : 0;        // the row's first partial slot
       const int mine = parts > 1 ? pair_rank[pl] - pair_rank[first_pair[sg.b]] : 0;
-      __nv_bfloat16* dst = parts > 1 ? part_out + (static_cast<size_t>(slot0 + mine) * kHeads + h) * kDc
-                                     : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
+      {
+        // out = bf16(O / l): into the output row, or (split rows) into the
+        // row's partial slot (number `mine` of the row's parts), which the
+        // merge kernel combines
+        __nv_bfloat16* dst = parts > 1 ? part_out + (static_cast<size_t>(slot0 + mine) * kHeads + h) * kDc
+                                       : p.out + (static_cast<size_t>(row) * kHeads + h) * kDc;
+        // two chunks per tensor-memory wait where the registers allow (bf16)
+        constexpr int kEpBatch = C::kThreads <= 384 ? 2 : 1;
 #pragma unroll 1
-      for (int cc = c0; cc < c0 + kEpChunks; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem + lane_base + 32u * cc, r);
-        ptx::tmem_wait_ld();
-        uint32_t o[16];
+        for (int cc = c0; cc < c0 + kEpChunks; cc += kEpBatch) {
+          uint32_t r[kEpBatch][32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-        ptx::st_global_v8(dst + cc * 32, o);          // whole 32-byte sectors
-        ptx::st_global_v8(dst + cc * 32 + 16, o + 8);
+          for (int k = 0; k < kEpBatch; ++k) ptx::tmem_ld32(tmem + lane_base + 32u * (cc + k), r[k]);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < kEpBatch; ++k) {
+            uint32_t o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o[e] = pack_bf16x2(__uint_as_float(r[k][2 * e]) * inv_l, __uint_as_float(r[k][2 * e + 1]) * inv_l);
+            ptx::st_global_v8(dst + (cc + k) * 32, o);          // whole 32-byte sectors
+            ptx::st_global_v8(dst + (cc + k) * 32 + 16, o + 8);
+          }
+        }
       }
-      if (parts > 1) count_written(merge_cnt + static_cast<size_t>(p.fp8_fallback) * p.L.max_slots + slot0, lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive(BAR(OEMPTY));
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_remote(ptx::mapa(BAR(MBEMPTY + ms), 1));
       if (++ms == kMailSlots) { ms = 0; mphase ^= 1u; }
-    }
-  }
-
-  // ------------------------------------------------------------ split-row merge
-  // Every warp of both CTAs, once its role is done: if this pair's last
-  // segment is part k < P-1 of a split row, merge heads [128k/(P-1),
-  // 128(k+1)/(P-1)) of that row (see merge_heads).
-  if (active && lo < hi && read_status(&hdr->abort_flag) == 0) {
-    const int bl = reinterpret_cast<const int*>(p.ws + p.L.pair_bl)[pl];   // the row holding page hi - 1
-    const int parts = n_parts[bl];
-    const int mine = parts > 1 ? pair_rank[pl] - pair_rank[first_pair[bl]] : 0;
-    if (parts > 1 && mine < parts - 1) {
-      const int slot0 = group * spq + slot_base[bl];
-      const int row = bl * sq + group;
-      const int nwarps = static_cast<int>(blockDim.x >> 5);
-      const uint32_t* cnt = merge_cnt + static_cast<size_t>(p.fp8_fallback) * p.L.max_slots + slot0;
-      if (wait_count(cnt, static_cast<uint32_t>(parts * (C::kEpWarps + 4)), hdr))
-        merge_heads<C::kThreads <= 384 ? 3 : 1>(part_out, part_lse, slot0, parts, kHeads * mine / (parts - 1), kHeads * (mine + 1) / (parts - 1),
-                    static_cast<int>(rank) * nwarps + warp, 2 * nwarps, lane,
-                    p.out + static_cast<size_t>(row) * kHeads * kDc, p.lse + static_cast<size_t>(row) * kHeads);
     }
   }
 

@@ -54,6 +54,8 @@ int decode_max_pairs();
 // W^UV up-projection of latent outputs (see wuv.cu).
 cudaError_t launch_wuv(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* o, const void* w, int rows, void* out,
                        void* hdr, cudaStream_t stream);
+cudaError_t launch_combine_plan(const void* ws, const WsLayout& Lw, int batch, int sq, __nv_bfloat16* out, float* lse,
+                                bool pdl, cudaStream_t stream);
 cudaError_t launch_combine_indptr(const float* part_out, const float* part_lse, const int32_t* indptr, int rows,
                                   __nv_bfloat16* out, float* lse, cudaStream_t stream);
 

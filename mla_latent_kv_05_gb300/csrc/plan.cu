@@ -14,10 +14,9 @@
 // query index i < Sq has its own group of pairs with the identical
 // partition, so the groups read the same pages at about the same time and
 // share them in L2.  A row covered by one pair is written straight to `out`;
-// a row covered by k > 1 pairs gets k partial slots (per query index), and
-// the attention kernel merges them (the part that finishes last does).  The
-// planner zeroes the merge counters and writes the rows that have no token
-// (out = 0, lse = -inf), which the attention kernel never visits.
+// a row covered by k > 1 pairs gets k partial slots (per query index),
+// which the merge kernel combines.  The planner writes the rows that have no
+// token (out = 0, lse = -inf), which neither kernel visits.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -78,12 +77,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   int* pair_lo = reinterpret_cast<int*>(ws + L.pair_lo);
   int* pair_rank = reinterpret_cast<int*>(ws + L.pair_rank);
   int* pair_b0 = reinterpret_cast<int*>(ws + L.pair_b0);
-  int* pair_bl = reinterpret_cast<int*>(ws + L.pair_bl);
   int* first_pair = reinterpret_cast<int*>(ws + L.first_pair);
   int* slot_base = reinterpret_cast<int*>(ws + L.slot_base);
   int* n_parts = reinterpret_cast<int*>(ws + L.n_parts);
   int* empty_rows = reinterpret_cast<int*>(ws + L.empty_rows);
-  int* merge_cnt = reinterpret_cast<int*>(ws + L.merge_cnt);
   const int ppg = pairs_per_group;
   int* s_lo = s_dyn;
   int* s_rank = s_dyn + (ppg + 1);
@@ -95,7 +92,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   // the attention kernel may begin its prologue now; it reads the plan only
   // after this grid has completed (griddepcontrol.wait)
   ptx::grid_dep_launch();
-  for (int i = tid; i < 2 * L.max_slots; i += blockDim.x) merge_cnt[i] = 0;
   const int per = (batch + blockDim.x - 1) / blockDim.x;
   const int lo = min(batch, tid * per), hi = min(batch, lo + per);
   const int max_len = max_pages * kPage;
@@ -166,21 +162,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
   }
   __syncthreads();
-  // pair_bl[p]: the row holding the pair's last page (where the pair ends,
-  // and whose split merge it may take part in); -1 for an empty range.
-  for (int pp = tid; pp < ppg; pp += blockDim.x) {
-    const int x = s_lo[pp + 1] - 1;
-    int l = -1;
-    if (x >= s_lo[pp]) {
-      int r = batch - 1;
-      l = 0;
-      while (l < r) {
-        const int mid = (l + r + 1) >> 1;
-        if (r_ts[mid] <= x) l = mid; else r = mid - 1;
-      }
-    }
-    pair_bl[pp] = l;
-  }
   // pair_rank[p]: pairs before p that have pages.  A pair range can be empty
   // (its cost share falls inside a row's start cost); a split row's parts
   // are the non-empty pairs over it, numbered by rank.
