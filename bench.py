@@ -398,6 +398,25 @@ def run_ours(args):
     st = binding.mla_get_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {binding.status_string(st)}")
+    graph_us = None
+    if args.workload == 1:
+        # The oracle-sized call is launch-latency bound: also time it replayed
+        # from a CUDA graph that captured one call (its three launches).
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        gb.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = ga.elapsed_time(gb) * 1000.0 / args.steps
+        if binding.mla_get_status(ws) != 0:
+            raise RuntimeError("device status after the graph replays")
     total_ms = float(np.sum(step_ms))
     total_ms_max = max_over_ranks(total_ms, world, dev)
     tokens_all = sum_over_ranks(float(counts["kv_tokens"] * args.steps), world, dev)
@@ -498,6 +517,7 @@ def run_ours(args):
                           "overlapping the neighbouring steps' calls); the KV cache stays resident in HBM"},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
+        **({"graph_us_per_call": graph_us} if graph_us is not None else {}),
         "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:

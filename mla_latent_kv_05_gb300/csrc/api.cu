@@ -73,6 +73,17 @@ int validate_common(const void* q_absorbed, const void* q_rope, const void* kv_c
 
 enum class CacheKind { kBf16, kFp8, kFp4 };
 
+// CTA pairs a query index gets: all resident pairs, but no more than one per
+// kPagesPerPair pages the call can hold (batch * max_pages, known on the host
+// without reading seq_lens).  A small decode then runs on a few pairs, and a
+// row of a few pages is not split (no partial write, nothing to merge).  The
+// workspace stays sized for all resident pairs.
+constexpr long long kPagesPerPair = 8;
+int pairs_for(int max_pairs, long long page_bound) {
+  const long long want = (page_bound + kPagesPerPair - 1) / kPagesPerPair;
+  return static_cast<int>(want < 1 ? 1 : (want < max_pairs ? want : max_pairs));
+}
+
 int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rope, const void* kv_cache,
                const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads, int num_pages,
                int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse, void* workspace,
@@ -84,7 +95,7 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int pairs = decode_max_pairs();
   if (pairs <= 0) return MLA_ERR_CUDA;
-  const int ppg = pairs / sq > 0 ? pairs / sq : 1;
+  const int ppg = pairs_for(pairs / sq > 0 ? pairs / sq : 1, static_cast<long long>(batch) * max_pages);
   const WsLayout L = ws_layout(batch, sq, pairs);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
@@ -199,10 +210,11 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   const WsLayout L = ws_layout(rows, 1, pairs, topk);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
   const int max_pages = (topk + kPage - 1) / kPage;
+  const int ppg = pairs_for(pairs, static_cast<long long>(rows) * max_pages);
   if (launch_sparse_prep(token_slots, rows, topk, num_pages * kPage, workspace, L, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   const int32_t* counts = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(workspace) + L.sp_lens);
-  if (launch_plan(counts, rows, 1, max_pages, pairs, workspace, L, reinterpret_cast<__nv_bfloat16*>(out), lse,
+  if (launch_plan(counts, rows, 1, max_pages, ppg, workspace, L, reinterpret_cast<__nv_bfloat16*>(out), lse,
                   stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   DecodeParams p;
@@ -213,7 +225,7 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   p.block_table = nullptr;
   p.batch = rows;
   p.sq = 1;
-  p.pairs_per_group = pairs;
+  p.pairs_per_group = ppg;
   p.num_pages = num_pages;
   p.max_pages = max_pages;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -227,7 +239,7 @@ int run_sparse(const uint16_t* q_absorbed, const uint16_t* q_rope, const void* k
   g_prof_before = g_prof_after = nullptr;
   const bool pdl = ev0 == nullptr;
   if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_decode_sparse(p, pairs, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode_sparse(p, ppg, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine_plan(workspace, L, rows, 1, p.out, lse, pdl, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;

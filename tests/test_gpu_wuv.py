@@ -59,5 +59,8 @@ def test_absorbed_decode_then_up_projection_equals_unabsorbed_attention(cuda_dev
         ref, _ = mla_oracle.attend_unabsorbed(q_nope[b, 0].double().numpy(), d.q_rope[b, 0].double().numpy(),
                                               c[:, :512], c[:, 512:], w_uk.double().numpy(),
                                               w_uv.double().numpy(), d.scale)
+        # the same bound as everywhere else: the GPU's roundings (the bf16
+        # absorbed query, the bf16 latent output, the bf16 result) give about
+        # 3e-3 to 5e-3 of max|ref| on these inputs
         err = np.abs(out[b, 0] - ref).max()
-        assert err <= 2e-2 * np.abs(ref).max(), (b, err)
+        assert err <= 1e-2 * np.abs(ref).max(), (b, err)
