@@ -104,6 +104,17 @@ def test_empty_rows_with_multi_token_queries(cuda_device):
     assert_close(out, lse, *oracle(inp))
 
 
+@pytest.mark.parametrize("sq,lens", [(1, [1, 70, 0, 130]), (2, [3, 65])])
+def test_wide_block_table_leaves_pairs_without_pages(cuda_device, sq, lens):
+    # a block table far wider than the rows: the call gets many CTA pairs
+    # (one per 8 pages it could hold) for a few pages, so most pair ranges
+    # are empty, and the rows that do have pages may be split between pairs
+    inp = gen.make_inputs(len(lens), sq, lens, seed=41 + sq, max_pages=96)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *oracle(inp))
+
+
 @pytest.mark.parametrize("sq,lens", [(1, [20000]), (2, [9000, 40])])
 def test_rows_split_over_many_pairs(cuda_device, sq, lens):
     # one long row cut into dozens of parts: the part that finishes last
