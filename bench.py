@@ -152,10 +152,25 @@ class ClockSampler:
                 "samples": len(rows), "samples_under_load": len(loaded)}
 
 
+def self_launch(gpus: int, argv) -> int:
+    """`--gpus N` (N > 1) with no launcher around this process: start N ranks,
+    one process per GPU, through torch.distributed.run on the loopback address
+    and return its exit status. Each rank then sees RANK, LOCAL_RANK and
+    WORLD_SIZE = N and runs the ordinary multi-rank path."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(gpus),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def dist_setup(gpus: int | None = None):
     """Rank, world size and local rank from the launcher's environment.
-    `--gpus N` must match the launcher's world size: N ranks are started by
-    torch.distributed.run (one process per GPU), never by this script, so a
+    `--gpus N` must match the launcher's world size (a run with no launcher and
+    N > 1 has already been re-started under one by `self_launch`), so a
     mismatch is an error rather than a silent one-GPU run."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -591,6 +606,8 @@ def main(argv=None):
     ap.add_argument("--wuv-rows", default=None,
                     help="time the W^UV up-projection alone on these row counts (e.g. 64,128,1024,4096)")
     args = ap.parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return self_launch(args.gpus, sys.argv[1:] if argv is None else list(argv))
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -39,13 +39,30 @@ def test_reference_arm_prints_the_contract_line(workload):
 
 
 def test_gpus_flag_must_match_the_launchers_world_size():
-    # --gpus 2 without a launcher that starts two ranks is an error, not a
-    # silent one-GPU run
+    # a launcher that started one rank while --gpus says two is an error, not
+    # a silent one-GPU run
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "LOCAL_RANK")}
+    env["WORLD_SIZE"] = "1"
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--workload", "1",
                         "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300,
-                       env={k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")})
+                       env=env)
     assert r.returncode != 0
     assert "WORLD_SIZE=1" in r.stderr
+
+
+def test_gpus_flag_without_a_launcher_starts_its_own_ranks():
+    # --gpus 2 with no launcher: bench.py re-starts itself under
+    # torch.distributed.run with two ranks (gloo here); the ranks' own world
+    # size check passes only if both were started, and rank 0 alone prints
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--workload", "1",
+                        "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["impl"] == "reference"
 
 
 def test_two_ranks_through_torchrun_print_one_line():
