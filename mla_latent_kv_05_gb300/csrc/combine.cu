@@ -98,53 +98,66 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // time; the parts are summed in slot order.
 __global__ void __launch_bounds__(256) combine_plan_kernel(const uint8_t* __restrict__ ws, WsLayout Lw, int sq,
                                                            __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  ptx::grid_dep_wait();
+  // The plan (part counts and slot bases) was written by the planner, which
+  // completed before the attention kernel let this grid launch, so it is read
+  // before the wait; the partials and their lse only after it.
   const int k = blockIdx.x;
   const int b = k / sq, i = k - b * sq;
-  const int parts = reinterpret_cast<const int*>(ws + Lw.n_parts)[b];
+  const int parts = __ldcg(reinterpret_cast<const int*>(ws + Lw.n_parts) + b);
+  const int base = __ldcg(reinterpret_cast<const int*>(ws + Lw.slot_base) + b);
+  const int spq = __ldcg(&reinterpret_cast<const PlanHeader*>(ws)->slots_per_query);
+  ptx::grid_dep_wait();
   if (parts <= 1) return;
-  const int spq = reinterpret_cast<const PlanHeader*>(ws)->slots_per_query;
-  const int start = i * spq + reinterpret_cast<const int*>(ws + Lw.slot_base)[b];
+  const int start = i * spq + base;
   const float* part_lse = reinterpret_cast<const float*>(ws + Lw.part_lse);
   const __nv_bfloat16* part_out = reinterpret_cast<const __nv_bfloat16*>(ws + Lw.part_out);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
-  float L = -INFINITY;
-  for (int s = lane; s < parts; s += 32) L = fmaxf(L, part_lse[static_cast<size_t>(start + s) * kHeads + h]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
   float acc[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-  float sum = 0.f;
-  if (L != -INFINITY) {
-    for (int s0 = 0; s0 < parts; s0 += 32) {
-      const int sl = s0 + lane;
-      const float v = sl < parts ? part_lse[static_cast<size_t>(start + sl) * kHeads + h] : -INFINITY;
-      const float wl = v == -INFINITY ? 0.f : __expf(v - L);
-      const int n = min(32, parts - s0);
-      for (int j0 = 0; j0 < n; j0 += 4) {
-        uint32_t x[4][8];
-        float wgt[4];
+  float sum = 0.f, L = -INFINITY;
+  // Parts in groups of 32 (one lse per lane); within a group the partial
+  // rows are read four at a time, and the first four are requested together
+  // with the group's lse values.  Each group's weights are taken against the
+  // running maximum, and earlier groups are rescaled when it grows.
+  for (int s0 = 0; s0 < parts; s0 += 32) {
+    const int n = min(32, parts - s0);
+    const int sl = s0 + lane;
+    const float v = sl < parts ? __ldcg(part_lse + static_cast<size_t>(start + sl) * kHeads + h) : -INFINITY;
+    uint32_t x[4][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wgt[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
-          if (j0 + u < n) {
+    for (int u = 0; u < 4; ++u)
+      if (u < n) ptx::ld_global_cg_v8(part_out + (static_cast<size_t>(start + s0 + u) * kHeads + h) * kDc + 16 * lane, x[u]);
+    float gm = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+    const float Ln = fmaxf(L, gm);
+    if (Ln != -INFINITY && L != Ln && L != -INFINITY) {
+      const float r = __expf(L - Ln);
+      sum *= r;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] *= r;
+    }
+    L = Ln;
+    const float wl = (v == -INFINITY || L == -INFINITY) ? 0.f : __expf(v - L);
+    for (int j0 = 0; j0 < n; j0 += 4) {
+      if (j0 > 0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j0 + u < n)
             ptx::ld_global_cg_v8(part_out + (static_cast<size_t>(start + s0 + j0 + u) * kHeads + h) * kDc + 16 * lane, x[u]);
-          } else {
-            wgt[u] = 0.f;
+      }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[u][e] = 0u;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          sum += wgt[u];
+      for (int u = 0; u < 4; ++u) {
+        const float wg = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
+        if (j0 + u < n) {
+          sum += wg;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[u][e]));
-            acc[2 * e] = fmaf(wgt[u], f.x, acc[2 * e]);
-            acc[2 * e + 1] = fmaf(wgt[u], f.y, acc[2 * e + 1]);
+            acc[2 * e] = fmaf(wg, f.x, acc[2 * e]);
+            acc[2 * e + 1] = fmaf(wg, f.y, acc[2 * e + 1]);
           }
         }
       }

@@ -1,6 +1,6 @@
 // Split-KV planner: turns seq_lens (on the device, no host sync) into an even
 // partition of KV tiles over the persistent CTA pairs and the partial-output
-// slots of rows that end up split.  One CTA of 1024 threads; the arrays it
+// slots of rows that end up split.  One CTA of 128 to 1024 threads; the arrays it
 // searches are mirrored in shared memory, because a chain of dependent
 // global reads would sit on the call's critical path (the attention kernel
 // waits for this grid).
@@ -282,7 +282,11 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_page
                         void* ws, const WsLayout& L, __nv_bfloat16* out, float* lse, cudaStream_t stream) {
   const size_t smem = sizeof(int) * (2 * static_cast<size_t>(pairs_per_group + 1) +
                                      (batch <= kPlanSmemRows ? 2 * static_cast<size_t>(batch + 1) : 0));
-  return launch_kernel(plan_kernel, dim3(1), dim3(1024), smem, stream, seq_lens, batch, sq, max_pages,
+  // one thread per row (or pair boundary), at least four warps: a small
+  // batch synchronises fewer warps at each of the planner's block barriers
+  const int want = batch > pairs_per_group + 1 ? batch : pairs_per_group + 1;
+  const int threads = want >= 1024 ? 1024 : (want <= 128 ? 128 : (want + 31) / 32 * 32);
+  return launch_kernel(plan_kernel, dim3(1), dim3(threads), smem, stream, seq_lens, batch, sq, max_pages,
                        pairs_per_group, static_cast<uint8_t*>(ws), L, out, lse);
 }
 
