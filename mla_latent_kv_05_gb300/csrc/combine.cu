@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(256) combine_plan_kernel(const uint8_t* __rest
   const int base = __ldcg(reinterpret_cast<const int*>(ws + Lw.slot_base) + b);
   const int spq = __ldcg(&reinterpret_cast<const PlanHeader*>(ws)->slots_per_query);
   ptx::grid_dep_wait();
+  // the next call's planner may begin launching (it waits for this grid
+  // before it reads or writes anything)
+  ptx::grid_dep_launch();
   if (parts <= 1) return;
   const int start = i * spq + base;
   const float* part_lse = reinterpret_cast<const float*>(ws + Lw.part_lse);

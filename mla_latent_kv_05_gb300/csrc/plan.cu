@@ -57,19 +57,57 @@ __device__ int block_exclusive_scan(int v, int* smem_warp, int* total) {
   return warp_excl + x - v;
 }
 
+// Exclusive block scan of two non-negative counts at once (one round of
+// barriers): a and b are packed into one 64-bit word, a in the high half.
+// Both sums stay below 2^31, as the planner's int totals already require, so
+// b never carries into a.
+__device__ void block_exclusive_scan2(int a, int b, unsigned long long* smem_warp, int* ex_a, int* ex_b, int* tot_a,
+                                      int* tot_b) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long v = (static_cast<unsigned long long>(static_cast<unsigned>(a)) << 32) |
+                               static_cast<unsigned>(b);
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = (lane < static_cast<int>(blockDim.x >> 5)) ? smem_warp[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem_warp[lane] = w;   // inclusive scan of warp totals
+  }
+  __syncthreads();
+  const unsigned long long ex = (warp > 0 ? smem_warp[warp - 1] : 0ull) + x - v;
+  const unsigned long long tot = smem_warp[(blockDim.x >> 5) - 1];
+  *ex_a = static_cast<int>(ex >> 32);
+  *ex_b = static_cast<int>(ex & 0xFFFFFFFFull);
+  *tot_a = static_cast<int>(tot >> 32);
+  *tot_b = static_cast<int>(tot & 0xFFFFFFFFull);
+  __syncthreads();
+}
+
 // Rows whose planner arrays (tile starts and costs) are kept in shared
 // memory while the planner searches them; larger batches search the global
 // copies instead (the same result, with longer dependent reads).
-constexpr int kPlanSmemRows = 4096;
+constexpr int kPlanSmemRows = 2048;   // 4 mirrors of [batch + 1] ints: 32 KiB, under the 48 KiB default
 
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens, int batch, int sq,
                                                     int max_pages, int pairs_per_group,
                                                     uint8_t* __restrict__ ws, WsLayout L,
                                                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   __shared__ int s_warp[32];
+  __shared__ unsigned long long s_warp2[32];
   __shared__ int s_chunk;
   // dynamic: pair_lo and pair_rank mirrors [ppg + 1] each, then (batch <=
-  // kPlanSmemRows) tile_start and row_cost mirrors [batch + 1] each
+  // kPlanSmemRows) tile_start and row_cost mirrors [batch + 1] each and the
+  // rows' clamped lengths and part counts [batch] each
   extern __shared__ int s_dyn[];
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
   int* lens = reinterpret_cast<int*>(ws + L.lens);
@@ -87,8 +125,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   const bool rows_in_smem = batch <= kPlanSmemRows;
   int* r_ts = rows_in_smem ? s_dyn + 2 * (ppg + 1) : tile_start;
   int* r_cost = rows_in_smem ? r_ts + (batch + 1) : reinterpret_cast<int*>(ws + L.row_cost);
+  int* r_len = rows_in_smem ? r_cost + (batch + 1) : lens;
+  int* r_parts = rows_in_smem ? r_len + batch : n_parts;
 
   const int tid = threadIdx.x;
+  // This grid is a programmatic dependent of whatever precedes it in the
+  // stream (seq_lens may come from it, and the previous call's merge kernel
+  // reads the plan arrays): nothing is read or written before the wait.
+  ptx::grid_dep_wait();
   // the attention kernel may begin its prologue now; it reads the plan only
   // after this grid has completed (griddepcontrol.wait)
   ptx::grid_dep_launch();
@@ -105,18 +149,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       s = s < 0 ? 0 : max_len;
     }
     lens[b] = s;
+    r_len[b] = s;
     local += (s + kPage - 1) / kPage;
     local_ne += s > 0 ? 1 : 0;
   }
-  int total = 0;
-  int excl = block_exclusive_scan(local, s_warp, &total);
   // Row costs for the partition: a row with pages costs its pages plus
   // kSegCost pages' worth for its segment start (query load, output write,
   // pipeline refill).
-  int ne_total = 0;
-  int ne_excl = block_exclusive_scan(local_ne, s_warp, &ne_total);
+  int total = 0, ne_total = 0, excl = 0, ne_excl = 0;
+  block_exclusive_scan2(local, local_ne, s_warp2, &excl, &ne_excl, &total, &ne_total);
   for (int b = lo; b < hi; ++b) {
-    const int n = (lens[b] + kPage - 1) / kPage;
+    const int n = (r_len[b] + kPage - 1) / kPage;
     r_ts[b] = excl;
     if (rows_in_smem) tile_start[b] = excl;
     r_cost[b] = excl + kSegCost * ne_excl;
@@ -198,7 +241,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   local = 0;
   int local_empty = 0;
   for (int b = lo; b < hi; ++b) {
-    const int n = (lens[b] + kPage - 1) / kPage;
+    const int n = (r_len[b] + kPage - 1) / kPage;
     int parts = 0, fp = 0;
     if (n > 0) {
       const int t0 = r_ts[b];
@@ -207,15 +250,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
     first_pair[b] = fp;
     n_parts[b] = parts;
+    r_parts[b] = parts;
     local += parts > 1 ? parts : 0;
     local_empty += parts == 0 ? 1 : 0;
   }
-  int slots_total = 0;
-  int slot_excl = block_exclusive_scan(local, s_warp, &slots_total);
-  int empty_total = 0;
-  int empty_excl = block_exclusive_scan(local_empty, s_warp, &empty_total);
+  int slots_total = 0, empty_total = 0, slot_excl = 0, empty_excl = 0;
+  block_exclusive_scan2(local, local_empty, s_warp2, &slot_excl, &empty_excl, &slots_total, &empty_total);
   for (int b = lo; b < hi; ++b) {
-    const int parts = n_parts[b];
+    const int parts = r_parts[b];
     slot_base[b] = parts > 1 ? slot_excl : -1;
     if (parts > 1) slot_excl += parts;
     if (parts == 0) empty_rows[empty_excl++] = b;
@@ -281,13 +323,25 @@ cudaError_t launch_sparse_prep(const int32_t* token_slots, int rows, int topk, i
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int sq, int max_pages, int pairs_per_group,
                         void* ws, const WsLayout& L, __nv_bfloat16* out, float* lse, cudaStream_t stream) {
   const size_t smem = sizeof(int) * (2 * static_cast<size_t>(pairs_per_group + 1) +
-                                     (batch <= kPlanSmemRows ? 2 * static_cast<size_t>(batch + 1) : 0));
+                                     (batch <= kPlanSmemRows ? 4 * static_cast<size_t>(batch + 1) : 0));
   // one thread per row (or pair boundary), at least four warps: a small
   // batch synchronises fewer warps at each of the planner's block barriers
   const int want = batch > pairs_per_group + 1 ? batch : pairs_per_group + 1;
   const int threads = want >= 1024 ? 1024 : (want <= 128 ? 128 : (want + 31) / 32 * 32);
-  return launch_kernel(plan_kernel, dim3(1), dim3(threads), smem, stream, seq_lens, batch, sq, max_pages,
-                       pairs_per_group, static_cast<uint8_t*>(ws), L, out, lse);
+  // a programmatic dependent of the previous kernel in the stream: its launch
+  // overlaps that kernel's tail, and it waits for it before reading anything
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, sq, max_pages, pairs_per_group,
+                            static_cast<uint8_t*>(ws), L, out, lse);
 }
 
 }  // namespace mla
