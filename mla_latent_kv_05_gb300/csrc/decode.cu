@@ -84,6 +84,7 @@ constexpr uint32_t kVSlot = 4 * 8 * kAtom;             // half page, eight laten
 constexpr uint32_t kVGroup = 8 * kAtom;                // row-group stride of a V slot
 constexpr uint32_t kPChunk = 128 * 128;                // 64 tokens of P for 128 heads (16 KiB)
 constexpr int kPSlots = 2;
+constexpr int kMaxSBufs = 3;   // S buffers in TMEM (per mode: Cfg::kSBufs)
 constexpr int kMailSlots = 2;
 constexpr int kHalf = kPage / 2;                        // tokens per half page
 constexpr uint32_t kRawBytes = kHalf * kFp8Row;         // raw FP8 half page: 19,008 B
@@ -103,6 +104,7 @@ constexpr int kMaxVSlots = 5, kMaxRaw = 4;
 template <int kMode> struct Cfg;
 template <> struct Cfg<0> {
   static constexpr int kTileHalves = 3;
+  static constexpr int kSBufs = 2;             // 2 x 96 columns of S beside Q's 288 + 32 spare
   static constexpr int kVSlots = 5;
   static constexpr uint32_t kPSlotBytes = 2 * kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;
@@ -119,6 +121,7 @@ template <> struct Cfg<0> {
 // FP8 modes: 1 = exact bf16 operands; 2 = f16 operands (same layout)
 template <> struct Cfg<1> {
   static constexpr int kTileHalves = 2;
+  static constexpr int kSBufs = 3;             // 3 x 64 columns: S runs a tile further ahead of the softmax
   static constexpr int kVSlots = 4;
   static constexpr uint32_t kPSlotBytes = kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;                       // rank 0
@@ -153,8 +156,8 @@ enum Bar {
   KFULLB = KEMPTY + 2, KEMPTYB = KFULLB + 2,   // bf16 score SM: the chunk 5..8 part of a tile
   VFULL = KEMPTYB + 2, VEMPTY = VFULL + kMaxVSlots,
   PFULL = VEMPTY + kMaxVSlots, PEMPTY = PFULL + kPSlots,
-  SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + 2,
-  QREADY = SEMPTY + 2, REQ, CORR, OFULL, OEMPTY, LSUM,
+  SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + kMaxSBufs,
+  QREADY = SEMPTY + kMaxSBufs, REQ, CORR, OFULL, OEMPTY, LSUM,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
   RAWFULL = MBEMPTY + kMailSlots, RAWEMPTY = RAWFULL + kMaxRaw,
   DRAIN = RAWEMPTY + kMaxRaw,   // the MMA issuer's last commit, waited for at teardown
@@ -172,7 +175,7 @@ static_assert(Cfg<0>::kOffMisc % 1024 == 0, "slot alignment");
 
 // TMEM columns.
 constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
-constexpr uint32_t kSCol = 320;    // rank 1: two S buffers of N columns (N <= 96)
+constexpr uint32_t kSCol = 320;    // rank 1: Cfg::kSBufs S buffers of N columns (up to column 512)
 constexpr uint32_t kTmemCols = 512;
 
 // P.V: A = P (K-major), B = V (MN-major); bf16, or f16 in the FP8 f16 mode
@@ -488,6 +491,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
   constexpr int kSG = C::kSmGroups;             // softmax warp groups
   constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
+  static_assert(C::kSBufs <= kMaxSBufs && kSCol + C::kSBufs * kN <= 512, "S buffers fit in TMEM");
   constexpr bool kQuant = kMode == 1 || kMode == 2 || kMode == 4 || kMode == 5;  // FP8 or FP4 cache (raw rings, dequant warps)
   constexpr bool kFp4 = kMode == 4 || kMode == 5;
   // a quantised row and the half page the producer copies (its ring slots
@@ -544,7 +548,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
       ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
     for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
-    for (int s = 0; s < 2; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128 * kSG); }
+    for (int s = 0; s < kMaxSBufs; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128 * kSG); }
     ptx::mbar_init(BAR(QREADY), 128 * kSG);
     ptx::mbar_init(BAR(REQ), 2);
     ptx::mbar_init(BAR(CORR), kEp);
@@ -979,7 +983,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
         __syncwarp();
         kb ^= 1;
         if (kb == 0) kphase ^= 1u;
-        if (++sb == 2) { sb = 0; sphase ^= 1u; }
+        if (++sb == C::kSBufs) { sb = 0; sphase ^= 1u; }
       }
     }
     // every MMA this thread issued completes before the CTA may leave
@@ -1215,7 +1219,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
         if (sends_alpha)
           ptx::st_async_v4(ptx::mapa(sbase + kOffAlpha + ps * 512u + (h + 3 * lane) * 4u, 0), __float_as_uint(a4[0]),
                            __float_as_uint(a4[1]), __float_as_uint(a4[2]), __float_as_uint(a4[3]), pfull);
-        if (++sb == 2) { sb = 0; sphase ^= 1u; }
+        if (++sb == C::kSBufs) { sb = 0; sphase ^= 1u; }
         if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
       }
       if (!ok) break;
