@@ -83,7 +83,7 @@ constexpr uint32_t kKB = 4 * 4 * kAtom;                // bf16 score SM: half pa
 constexpr uint32_t kVSlot = 4 * 8 * kAtom;             // half page, eight latent chunks (32 KiB)
 constexpr uint32_t kVGroup = 8 * kAtom;                // row-group stride of a V slot
 constexpr uint32_t kPChunk = 128 * 128;                // 64 tokens of P for 128 heads (16 KiB)
-constexpr int kPSlots = 2;
+constexpr int kMaxPSlots = 3;  // P slots on the value SM (per mode: Cfg::kPSlots)
 constexpr int kMaxSBufs = 3;   // S buffers in TMEM (per mode: Cfg::kSBufs)
 constexpr int kMailSlots = 2;
 constexpr int kHalf = kPage / 2;                        // tokens per half page
@@ -97,8 +97,8 @@ constexpr int kMaxVSlots = 5, kMaxRaw = 4;
 //         slots of two chunks (96 tokens).
 //   FP8:  each SM bulk-loads every raw half page (the second read is an L2
 //         hit) and dequantises what its own MMAs read: rank 1 = 4 K slots
-//         (two 2-slot tiles) + 4 raw half pages; rank 0 = 4 V slots + 2
-//         one-chunk P slots + 3 raw half pages.  Moving dequantised rows
+//         (two 2-slot tiles) + 4 raw half pages; rank 0 = 4 V slots + 3
+//         one-chunk P slots + 2 raw half pages.  Moving dequantised rows
 //         between the two SMs instead would cost more: shared-to-shared
 //         traffic inside a cluster runs at about 42 GB/s per pair on GB300.
 template <int kMode> struct Cfg;
@@ -106,6 +106,7 @@ template <> struct Cfg<0> {
   static constexpr int kTileHalves = 3;
   static constexpr int kSBufs = 2;             // 2 x 96 columns of S beside Q's 288 + 32 spare
   static constexpr int kVSlots = 5;
+  static constexpr int kPSlots = 2;
   static constexpr uint32_t kPSlotBytes = 2 * kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;
   static constexpr int kRaw0 = 0, kRaw1 = 0;
@@ -123,9 +124,10 @@ template <> struct Cfg<1> {
   static constexpr int kTileHalves = 2;
   static constexpr int kSBufs = 3;             // 3 x 64 columns: S runs a tile further ahead of the softmax
   static constexpr int kVSlots = 4;
+  static constexpr int kPSlots = 3;            // and P a tile further ahead of P.V
   static constexpr uint32_t kPSlotBytes = kPChunk;
   static constexpr uint32_t kOffP = kVSlots * kVSlot;                       // rank 0
-  static constexpr int kRaw0 = 3, kRaw1 = 4;
+  static constexpr int kRaw0 = 2, kRaw1 = 4;
   static constexpr uint32_t kOffRaw0 = kOffP + kPSlots * kPSlotBytes;       // rank 0
   static constexpr uint32_t kOffRaw1 = 2 * kTileHalves * kKSlot;            // rank 1: after the K slots
   static constexpr uint32_t kEnd1 = kOffRaw1 + kRaw1 * kRawBytes;
@@ -145,18 +147,18 @@ template <> struct Cfg<5> : Cfg<1> {};
 // sparse decode over the bf16 cache: the bf16 plan, K and V gathered by rows
 template <> struct Cfg<3> : Cfg<0> {};
 constexpr int kGatherWarps = 3;          // sparse: warps 0, 2, 3 of each rank copy one half page of a tile each
-constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [2][128]
+constexpr uint32_t kMiscAlpha = 0;       // rank 0: fp32 alpha [kMaxPSlots][128]
 constexpr uint32_t kMiscLPart = 0;       // rank 1 (same bytes): group-1 partial softmax sums [128]
-constexpr uint32_t kMiscMail = 1024;     // rank 0: fp32 1/l [2][128]
-constexpr uint32_t kMiscReq = 2048;      // rank 0: P slot of a rescale request
-constexpr uint32_t kMiscRawFlag = 2064;  // per raw stage: 1 = write zeros (bad page)
+constexpr uint32_t kMiscMail = 512 * kMaxPSlots;   // rank 0: fp32 1/l [2][128]
+constexpr uint32_t kMiscReq = kMiscMail + 1024;    // rank 0: P slot of a rescale request
+constexpr uint32_t kMiscRawFlag = kMiscReq + 16;   // per raw stage: 1 = write zeros (bad page)
 constexpr uint32_t kMiscBar = kMiscRawFlag + 4 * kMaxRaw;
 enum Bar {
   KFULL = 0, KEMPTY = KFULL + 2,
   KFULLB = KEMPTY + 2, KEMPTYB = KFULLB + 2,   // bf16 score SM: the chunk 5..8 part of a tile
   VFULL = KEMPTYB + 2, VEMPTY = VFULL + kMaxVSlots,
-  PFULL = VEMPTY + kMaxVSlots, PEMPTY = PFULL + kPSlots,
-  SFULL = PEMPTY + kPSlots, SEMPTY = SFULL + kMaxSBufs,
+  PFULL = VEMPTY + kMaxVSlots, PEMPTY = PFULL + kMaxPSlots,
+  SFULL = PEMPTY + kMaxPSlots, SEMPTY = SFULL + kMaxSBufs,
   QREADY = SEMPTY + kMaxSBufs, REQ, CORR, OFULL, OEMPTY, LSUM,
   MBFULL, MBEMPTY = MBFULL + kMailSlots,
   RAWFULL = MBEMPTY + kMailSlots, RAWEMPTY = RAWFULL + kMaxRaw,
@@ -492,6 +494,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
   constexpr int kHC = kN / kSG;                 // S columns per softmax group
   constexpr int kVSlots = C::kVSlots;
   static_assert(C::kSBufs <= kMaxSBufs && kSCol + C::kSBufs * kN <= 512, "S buffers fit in TMEM");
+  static_assert(C::kPSlots <= kMaxPSlots, "P slots and their alpha rows");
   constexpr bool kQuant = kMode == 1 || kMode == 2 || kMode == 4 || kMode == 5;  // FP8 or FP4 cache (raw rings, dequant warps)
   constexpr bool kFp4 = kMode == 4 || kMode == 5;
   // a quantised row and the half page the producer copies (its ring slots
@@ -547,7 +550,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
       ptx::mbar_init(BAR(VFULL + s), kQuant ? dq : (kMode == 3 ? 32u : 1u));   // sparse: one warp per half page
       ptx::mbar_init(BAR(VEMPTY + s), 1);
     }
-    for (int s = 0; s < kPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
+    for (int s = 0; s < kMaxPSlots; ++s) { ptx::mbar_init(BAR(PFULL + s), 128 * kSG); ptx::mbar_init(BAR(PEMPTY + s), 1); }
     for (int s = 0; s < kMaxSBufs; ++s) { ptx::mbar_init(BAR(SFULL + s), 1); ptx::mbar_init(BAR(SEMPTY + s), 128 * kSG); }
     ptx::mbar_init(BAR(QREADY), 128 * kSG);
     ptx::mbar_init(BAR(REQ), 2);
@@ -1073,7 +1076,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
           if (h0 + TH >= hp_end) ptx::mma_commit(BAR(OFULL));
         }
         __syncwarp();
-        if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
+        if (++ps == C::kPSlots) { ps = 0; pphase ^= 1u; }
       }
       first_seg = false;
     }
@@ -1220,7 +1223,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
           ptx::st_async_v4(ptx::mapa(sbase + kOffAlpha + ps * 512u + (h + 3 * lane) * 4u, 0), __float_as_uint(a4[0]),
                            __float_as_uint(a4[1]), __float_as_uint(a4[2]), __float_as_uint(a4[3]), pfull);
         if (++sb == C::kSBufs) { sb = 0; sphase ^= 1u; }
-        if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
+        if (++ps == C::kPSlots) { ps = 0; pphase ^= 1u; }
       }
       if (!ok) break;
       if (kSG == 2 && grp == 1) {
@@ -1252,9 +1255,9 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
     }
     // the last remote arrivals from rank 0 must land before this CTA exits
     if (ok && grp == 0) {
-      for (int s = 0; s < kPSlots && ok; ++s) {
+      for (int s = 0; s < C::kPSlots && ok; ++s) {
         ok = wait_warp<true>(BAR(PEMPTY + ps), pphase ^ 1u, hdr);
-        if (++ps == kPSlots) { ps = 0; pphase ^= 1u; }
+        if (++ps == C::kPSlots) { ps = 0; pphase ^= 1u; }
       }
       for (int s = 0; s < kMailSlots && ok; ++s) {
         ok = wait_warp<true>(BAR(MBEMPTY + ms), mphase ^ 1u, hdr);
