@@ -117,12 +117,41 @@ def test_wide_block_table_leaves_pairs_without_pages(cuda_device, sq, lens):
 
 @pytest.mark.parametrize("sq,lens", [(1, [20000]), (2, [9000, 40])])
 def test_rows_split_over_many_pairs(cuda_device, sq, lens):
-    # one long row cut into dozens of parts: the part that finishes last
-    # merges all the others' partials with its own output
+    # one long row cut into dozens of parts (40 for the 20000-token row, so
+    # the merge kernel takes their lse values in two groups of up to 32)
     inp = gen.make_inputs(len(lens), sq, lens, seed=31 + sq)
     out, lse, st = run_gpu(inp)
     assert st == 0
     assert_close(out, lse, *oracle(inp))
+
+
+def test_lengths_written_just_before_the_call_are_used(cuda_device):
+    # The planner is launched as a programmatic dependent of whatever precedes
+    # it on the stream: lengths that a device kernel writes immediately before
+    # the call (here the reversed list, capped at 1000) must be the ones it
+    # plans with, and a second call with the original lengths must not see
+    # stale plan state from the first.  Every row's block table covers both.
+    lens = [300, 1, 0, 2000, 777, 64, 65, 1500]
+    new = [min(x, 1000) for x in lens[::-1]]
+    alloc = [max(a, b) for a, b in zip(lens, new)]
+    inp = gen.make_inputs(len(lens), 1, alloc, seed=61)
+    d = to_dev(inp)
+    ws = binding.alloc_workspace(inp.batch, inp.sq)
+    orig = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    sl = torch.minimum(orig.flip(0), torch.full_like(orig, 1000))   # device kernels on the call's stream
+    raw = inp.kv_cache.double().numpy()
+    rows = mla_oracle.cache_rows(raw, "bf16")
+
+    def ref(lengths):
+        return mla_oracle.mla_decode(inp.q_absorbed.double().numpy(), inp.q_rope.double().numpy(), rows,
+                                     inp.block_table.numpy(), np.array(lengths, dtype=np.int64), inp.scale)
+
+    out, lse = binding.mla_decode_bf16(d["q"], d["qr"], d["kv"], d["bt"], sl, inp.scale, workspace=ws)
+    assert binding.mla_get_status(ws) == 0
+    assert_close(out, lse, *ref(new))
+    out2, lse2 = binding.mla_decode_bf16(d["q"], d["qr"], d["kv"], d["bt"], orig, inp.scale, workspace=ws)
+    assert binding.mla_get_status(ws) == 0
+    assert_close(out2, lse2, *ref(lens))
 
 
 def test_single_token_is_bit_exact_copy(cuda_device):
