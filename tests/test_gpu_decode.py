@@ -125,6 +125,33 @@ def test_rows_split_over_many_pairs(cuda_device, sq, lens):
     assert_close(out, lse, *oracle(inp))
 
 
+def test_large_batch_plans_from_global_memory(cuda_device):
+    # 3000 rows (more than the planner mirrors in shared memory, so it
+    # searches its global arrays; three rows per planner thread), short
+    # random lengths with some empty rows.  Sampled rows are checked against
+    # the oracle (on just their pages), every empty row for out = 0 and
+    # lse = -inf.
+    rng = np.random.default_rng(71)
+    lens = rng.integers(0, 300, size=3000)
+    lens[rng.choice(3000, 40, replace=False)] = 0
+    inp = gen.make_inputs(3000, 1, lens.tolist(), seed=71)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    sample = np.array(sorted(set(rng.choice(3000, 48, replace=False).tolist()) | {0, 1, 2997, 2998, 2999}))
+    bt = inp.block_table.numpy()[sample]
+    used = np.unique(bt[bt >= 0])
+    remap = {int(p): k for k, p in enumerate(used)}
+    bt_sub = np.vectorize(lambda p: remap.get(int(p), -1))(bt).astype(np.int64)
+    rows = mla_oracle.cache_rows(inp.kv_cache[torch.as_tensor(used)].double().numpy(), "bf16")
+    ref_out, ref_lse = mla_oracle.mla_decode(inp.q_absorbed[sample].double().numpy(),
+                                             inp.q_rope[sample].double().numpy(), rows, bt_sub,
+                                             lens[sample], inp.scale)
+    assert_close(out[torch.as_tensor(sample)], lse[torch.as_tensor(sample)], ref_out, ref_lse)
+    empty = torch.as_tensor(np.nonzero(lens == 0)[0])
+    assert torch.all(out[empty].float() == 0)
+    assert torch.all(torch.isneginf(lse[empty]))
+
+
 def test_lengths_written_just_before_the_call_are_used(cuda_device):
     # The planner is launched as a programmatic dependent of whatever precedes
     # it on the stream: lengths that a device kernel writes immediately before
