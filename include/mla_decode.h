@@ -41,6 +41,15 @@
  * Tokens past seq_len inside a row's last page are ignored whatever they
  * hold (including NaN).
  *
+ * Stream order: the decode calls' kernels are chained with programmatic
+ * dependent launch.  The first one (the planner) is launched as a
+ * programmatic dependent of whatever precedes it on `stream` and waits for
+ * it before reading any input, so inputs written by earlier work on the
+ * stream are always seen.  The last one (the merge) lets a programmatic
+ * dependent that follows it begin launching early; such a kernel must wait
+ * for its predecessor (griddepcontrol.wait) before reading out or lse, as
+ * programmatic dependent launch requires of any kernel.
+ *
  * Errors: host-side validation failures return a negative mla_status before
  * anything is launched.  Launch failures return MLA_ERR_CUDA.  Problems only
  * the device can see (a block-table entry outside [0, num_pages), a
