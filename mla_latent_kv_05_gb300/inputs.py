@@ -30,12 +30,15 @@ FP8_ROW_BYTES = ROW_ELEMS + FP8_NUM_SCALES      # 594
 FP4_SCALE_GROUP = 16
 FP4_NUM_SCALES = ROW_ELEMS // FP4_SCALE_GROUP   # 36
 FP4_ROW_BYTES = ROW_ELEMS // 2 + FP4_NUM_SCALES # 324
+V41_VALUES = 512                                # V4.1 row: 448 latent + 64 RoPE values
+V41_NUM_SCALES = V41_VALUES // FP8_SCALE_GROUP  # 16
+V41_ROW_BYTES = V41_VALUES + V41_NUM_SCALES     # 528
 DEFAULT_SCALE = 1.0 / math.sqrt(128 + 64)       # 1/sqrt(d_h + d_h^R)
 
 
 def row_bytes_of(kv_dtype: str) -> int:
     """Bytes of one cached token row in each cache format."""
-    return {"bf16": ROW_ELEMS * 2, "fp8": FP8_ROW_BYTES, "fp4": FP4_ROW_BYTES}[kv_dtype]
+    return {"bf16": ROW_ELEMS * 2, "fp8": FP8_ROW_BYTES, "fp4": FP4_ROW_BYTES, "fp8v41": V41_ROW_BYTES}[kv_dtype]
 
 
 @dataclass
@@ -43,11 +46,11 @@ class DecodeInputs:
     """One decode call's inputs, on the host (CPU tensors)."""
     q_absorbed: torch.Tensor   # [B, Sq, H, 512] bf16
     q_rope: torch.Tensor       # [B, Sq, H, 64] bf16
-    kv_cache: torch.Tensor     # bf16 [P, 64, 576], uint8 [P, 64, 594] (fp8) or [P, 64, 324] (fp4)
+    kv_cache: torch.Tensor     # bf16 [P, 64, 576], uint8 [P, 64, 594] (fp8), [P, 64, 528] (fp8v41) or [P, 64, 324] (fp4)
     block_table: torch.Tensor  # int32 [B, max_pages], -1 where unused
     seq_lens: torch.Tensor     # int32 [B]
     scale: float
-    kv_dtype: str              # "bf16", "fp8" or "fp4"
+    kv_dtype: str              # "bf16", "fp8", "fp8v41" or "fp4"
     name: str = ""
     meta: dict = field(default_factory=dict)
 
@@ -83,6 +86,8 @@ WORKLOADS = {
             kv_dtype="bf16"),
     7: dict(name="fp4 B128 seq8192", batch=128, sq=1, seq=8192,
             kv_dtype="fp4"),
+    8: dict(name="fp8 V4.1 row B128 seq8192", batch=128, sq=1, seq=8192,
+            kv_dtype="fp8v41"),
 }
 
 
@@ -114,6 +119,22 @@ def _fp8_cache(gen: torch.Generator, num_pages: int, page_size: int) -> torch.Te
         out[p0:p1, :, :ROW_ELEMS] = vals.to(torch.float8_e4m3fn).view(torch.uint8)
         out[p0:p1, :, ROW_ELEMS:] = torch.randint(
             120, 131, (p1 - p0, page_size, FP8_NUM_SCALES), generator=gen,
+            dtype=torch.int64).to(torch.uint8)
+    return out
+
+
+def _fp8v41_cache(gen: torch.Generator, num_pages: int, page_size: int) -> torch.Tensor:
+    """[P, page, 528] uint8 V4.1 rows: 512 e4m3 bytes (N(0,1) rounded by
+    torch's cast; 448 latent then 64 RoPE values) followed by 16 e8m0
+    exponent bytes drawn uniformly from [120, 130]."""
+    out = torch.empty((num_pages, page_size, V41_ROW_BYTES), dtype=torch.uint8)
+    step = 512
+    for p0 in range(0, num_pages, step):
+        p1 = min(num_pages, p0 + step)
+        vals = torch.randn((p1 - p0, page_size, V41_VALUES), generator=gen)
+        out[p0:p1, :, :V41_VALUES] = vals.to(torch.float8_e4m3fn).view(torch.uint8)
+        out[p0:p1, :, V41_VALUES:] = torch.randint(
+            120, 131, (p1 - p0, page_size, V41_NUM_SCALES), generator=gen,
             dtype=torch.int64).to(torch.uint8)
     return out
 
@@ -169,6 +190,8 @@ def make_inputs(batch: int, sq: int, seq_lens, kv_dtype: str = "bf16",
         cache = _fp8_cache(gen, n_phys, page_size)
     elif kv_dtype == "fp4":
         cache = _fp4_cache(gen, n_phys, page_size)
+    elif kv_dtype == "fp8v41":
+        cache = _fp8v41_cache(gen, n_phys, page_size)
     else:
         raise ValueError(kv_dtype)
     return DecodeInputs(q_absorbed=q_abs, q_rope=q_rope, kv_cache=cache,

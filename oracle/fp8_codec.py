@@ -17,6 +17,13 @@ Format facts used:
 Row layout (the reading taken for the 594-byte row): bytes [0, 576) are the
 e4m3 codes of the 576 values (512 latent, then 64 RoPE), bytes [576, 594) are
 18 e8m0 scales, scale k covering values [32k, 32k+32).
+
+The V4.1 row (same record, same constraint (2)): 528 bytes per token, 512
+e4m3 codes "over all 512 dims", the 64 RoPE dims quantized too, then 16 e8m0
+scales, one per 32 codes.  Reading taken: its 512 values are 448 latent
+values followed by the 64 RoPE values (the same order as the 576-value row),
+scale k covering values [32k, 32k+32).  On this path's 576-value row the
+V4.1 latent occupies dims [0, 448); dims [448, 512) are zero.
 """
 from __future__ import annotations
 
@@ -26,6 +33,11 @@ ROW_VALUES = 576
 SCALE_GROUP = 32
 NUM_SCALES = ROW_VALUES // SCALE_GROUP
 ROW_BYTES = ROW_VALUES + NUM_SCALES
+
+V41_VALUES = 512                          # 448 latent + 64 RoPE
+V41_LATENT = 448
+V41_NUM_SCALES = V41_VALUES // SCALE_GROUP  # 16
+V41_ROW_BYTES = V41_VALUES + V41_NUM_SCALES  # 528
 
 
 def e4m3fn_to_float64(codes: np.ndarray) -> np.ndarray:
@@ -56,3 +68,19 @@ def dequant_rows(raw: np.ndarray) -> np.ndarray:
     vals = e4m3fn_to_float64(raw[..., :ROW_VALUES])
     scales = e8m0_to_float64(raw[..., ROW_VALUES:])
     return vals * np.repeat(scales, SCALE_GROUP, axis=-1)
+
+
+def dequant_rows_v41(raw: np.ndarray) -> np.ndarray:
+    """[..., 528] uint8 V4.1 rows -> [..., 576] float64 values on this path's
+    row: dims [0, 448) are the V4.1 latent, [448, 512) zero, [512, 576) the
+    RoPE values.  value[k] = e4m3(byte[k]) * e8m0(byte[512 + k // 32])."""
+    raw = np.asarray(raw, dtype=np.uint8)
+    assert raw.shape[-1] == V41_ROW_BYTES, raw.shape
+    vals = e4m3fn_to_float64(raw[..., :V41_VALUES])
+    scales = e8m0_to_float64(raw[..., V41_VALUES:])
+    v = vals * np.repeat(scales, SCALE_GROUP, axis=-1)
+    out = np.zeros(raw.shape[:-1] + (ROW_VALUES,), dtype=np.float64)
+    out[..., :V41_LATENT] = v[..., :V41_LATENT]
+    out[..., ROW_VALUES - (V41_VALUES - V41_LATENT):] = v[..., V41_LATENT:]
+    return out
+

@@ -32,7 +32,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fp8_codec import dequant_rows
+from .fp8_codec import dequant_rows, dequant_rows_v41
 from . import fp4_codec
 
 D_LATENT = 512
@@ -47,9 +47,12 @@ def visible_len(seq_len: int, sq: int, i: int) -> int:
 
 def cache_rows(kv_cache: np.ndarray, kv_dtype: str) -> np.ndarray:
     """The cache as float64 rows [P, page, 576]: bf16 caches arrive already
-    widened to float64 by the caller; FP8 and FP4 caches are decoded here."""
+    widened to float64 by the caller; FP8 (594- and 528-byte rows) and FP4
+    caches are decoded here."""
     if kv_dtype == "fp8":
         return dequant_rows(kv_cache)
+    if kv_dtype == "fp8v41":
+        return dequant_rows_v41(kv_cache)
     if kv_dtype == "fp4":
         return fp4_codec.dequant_rows(kv_cache)
     arr = np.asarray(kv_cache, dtype=np.float64)

@@ -92,6 +92,50 @@ def test_fp8_row_dequant_layout_against_torch():
     assert np.array_equal(as_bf16, mine)
 
 
+def test_v41_row_is_the_printed_528_bytes():
+    # "DeepSeek-R1" record, constraint (2): 512 e4m3 values plus 16 e8m0
+    # scales, one per 32 values, make the 528-byte V4.1 row
+    assert cf.fp8_row_bytes(512) == 528 == fp8_codec.V41_ROW_BYTES
+    assert fp8_codec.V41_NUM_SCALES == 16 and fp8_codec.V41_LATENT + 64 == fp8_codec.V41_VALUES
+
+
+def test_v41_row_layout_by_hand():
+    # codes all 1.0 (0x38), scale of group k = 2^(k - 7): value k of the V4.1
+    # row is 2^(k//32 - 7); latent values land in dims [0, 448), the RoPE
+    # values (the row's last 64) in dims [512, 576), and dims [448, 512) are 0
+    row = np.zeros(528, dtype=np.uint8)
+    row[:512] = 0x38
+    row[512:] = 120 + np.arange(16)
+    got = fp8_codec.dequant_rows_v41(row)
+    want = np.zeros(576)
+    v = 2.0 ** (np.arange(512) // 32 - 7)
+    want[:448] = v[:448]
+    want[512:] = v[448:]
+    assert np.array_equal(got, want)
+    assert got[447] == 2.0 ** 6 and got[448] == 0 and got[511] == 0 and got[512] == 2.0 ** 7 and got[575] == 2.0 ** 8
+
+
+def test_v41_rows_equal_the_594_byte_rows_they_embed_in():
+    # a V4.1 row and the 594-byte row with the same latent and RoPE values
+    # (zero codes for dims 448..511) decode to the same 576 values
+    inp = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp8v41", seed=5)
+    raw = inp.kv_cache.numpy()
+    wide = np.zeros(raw.shape[:-1] + (594,), dtype=np.uint8)
+    wide[..., :448] = raw[..., :448]
+    wide[..., 512:576] = raw[..., 448:512]
+    wide[..., 576:590] = raw[..., 512:526]          # scales of latent groups 0..13
+    wide[..., 590:592] = 127                         # groups 14, 15: zero codes, any scale
+    wide[..., 592:594] = raw[..., 526:528]          # scales of the RoPE groups
+    assert np.array_equal(fp8_codec.dequant_rows_v41(raw), fp8_codec.dequant_rows(wide))
+    # and against torch's own casts of the same bytes
+    v = torch.from_numpy(raw[..., :512].copy()).view(torch.float8_e4m3fn).to(torch.float64)
+    sc = torch.from_numpy(raw[..., 512:].copy()).view(torch.float8_e8m0fnu).to(torch.float64)
+    vals = (v * sc.repeat_interleave(32, dim=-1)).numpy()
+    got = fp8_codec.dequant_rows_v41(raw)
+    assert np.array_equal(got[..., :448], vals[..., :448]) and np.array_equal(got[..., 512:], vals[..., 448:])
+    assert not got[..., 448:512].any()
+
+
 def test_e2m1_table_is_the_ocp_value_set():
     # OCP MX FP4 E2M1: the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 in
     # code order, the sign bit negating them; no NaN or infinity
