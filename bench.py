@@ -351,7 +351,7 @@ def run_ours(args):
     else:
         counts = gen.workload_counts(inp)
         decode = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8,
-                  "fp4": binding.mla_decode_fp4}[inp.kv_dtype]
+                  "fp4": binding.mla_decode_fp4, "fp8v41": binding.mla_decode_fp8_v41}[inp.kv_dtype]
         bt = inp.block_table.to(dev)
         sl = inp.seq_lens.to(dev)
         ws = binding.alloc_workspace(inp.batch, inp.sq, dev)

@@ -175,6 +175,27 @@ int mla_decode_fp4(const uint16_t* q_absorbed, const uint16_t* q_rope,
                    float softmax_scale, uint16_t* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Same over an FP8 cache in the V4.1 row layout [num_pages, 64, 528]
+ * (uint8; "DeepSeek-R1" model record, engine kernel constraint (2): 512
+ * e4m3 values over all 512 dims, the 64 RoPE dims quantised too, then 16
+ * e8m0 scales, one per 32 values).  Reading taken: the 512 values are 448
+ * latent values followed by the 64 RoPE values:
+ *   v[k] = e4m3(byte[k]) * 2^(byte[512 + k/32] - 127),
+ * latent = v[0..447], RoPE key = v[448..511].  The call runs on the
+ * 512-value latent layout of the other entry points with latent dims
+ * [448, 512) taken as zero: q_absorbed keeps its [.., 512] shape and its
+ * dims 448..511 are ignored (read as zero, whatever they hold), and out
+ * dims 448..511 are written as 0.  Exactness, the f16-operand pass and its
+ * fallback are those of mla_decode_fp8; kv_cache must be 16-byte aligned.
+ * Arguments, layouts, results and errors are otherwise those of
+ * mla_decode_bf16. */
+int mla_decode_fp8_v41(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                       const uint8_t* kv_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, int batch, int sq, int num_heads,
+                       int num_pages, int page_size, int max_pages,
+                       float softmax_scale, uint16_t* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Sparse top-k decode ("DeepSeek-V3.2" model record: the sparse attention
  * indexer, index_topk 2048, selects the candidate tokens each query attends
  * over; the latent rows stay cached per token).  Query row (b, i) attends

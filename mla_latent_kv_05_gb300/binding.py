@@ -34,6 +34,8 @@ SIGNATURES = {
                             ctypes.c_size_t, _P]),
     "mla_decode_fp4": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                             ctypes.c_size_t, _P]),
+    "mla_decode_fp8_v41": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                                ctypes.c_size_t, _P]),
     "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_decode_sparse_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
@@ -206,6 +208,17 @@ def mla_decode_fp4(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, o
     36 e8m0 scales, one per 16 values); returns (out, lse)."""
     return _decode("mla_decode_fp4", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
                    workspace, stream, torch.uint8, 324)
+
+
+def mla_decode_fp8_v41(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out=None, lse=None,
+                       workspace=None, stream=None):
+    """MLA decode over an FP8 latent cache in the V4.1 row layout
+    [num_pages, 64, 528] (uint8 rows: 512 e4m3 codes, 448 latent then 64
+    RoPE, then 16 e8m0 scales, one per 32 codes); returns (out, lse) with
+    out [..., 512] whose dims 448..511 are 0 (q_absorbed dims 448..511 are
+    ignored)."""
+    return _decode("mla_decode_fp8_v41", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
+                   workspace, stream, torch.uint8, 528)
 
 
 def mla_workspace_size_sparse(batch: int, sq: int, topk: int, num_heads: int = 128, page_size: int = 64) -> int:

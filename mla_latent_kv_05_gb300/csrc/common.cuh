@@ -19,6 +19,12 @@ constexpr int kPage = 64;           // tokens per page (= tokens per KV tile)
 constexpr int kFp8Row = kRow + kRow / 32;   // 594 bytes
 constexpr int kFp4Codes = kRow / 2;         // FP4 row: 288 bytes of e2m1 codes (two per byte) ...
 constexpr int kFp4Row = kFp4Codes + kRow / 16;   // ... then 36 e8m0 scales (one per 16 values): 324 bytes
+// FP8 V4.1 row: 512 e4m3 codes (448 latent, then the 64 RoPE values) and 16
+// e8m0 scales (one per 32 codes): 528 bytes.  On the 576-value row the V4.1
+// latent fills dims [0, 448) and dims [448, 512) are zero.
+constexpr int kV41Values = 512;
+constexpr int kV41Latent = 448;
+constexpr int kV41Row = kV41Values + kV41Values / 32;   // 528 bytes
 constexpr int kMaxSq = 4;
 constexpr int kMaxRows = 1 << 16;   // batch * Sq handled by the planner
 

@@ -144,6 +144,10 @@ template <> struct Cfg<2> : Cfg<1> {};
 // operands (exact), 5 = f16 operands
 template <> struct Cfg<4> : Cfg<1> {};
 template <> struct Cfg<5> : Cfg<1> {};
+// FP8 V4.1 cache (528-byte rows): the FP8 roles and layout; 6 = bf16
+// operands (exact), 7 = f16 operands
+template <> struct Cfg<6> : Cfg<1> {};
+template <> struct Cfg<7> : Cfg<1> {};
 // sparse decode over the bf16 cache: the bf16 plan, K and V gathered by rows
 template <> struct Cfg<3> : Cfg<0> {};
 constexpr int kGatherWarps = 3;          // sparse: warps 0, 2, 3 of each rank copy one half page of a tile each
@@ -180,16 +184,23 @@ constexpr uint32_t kQCol = 0;      // rank 1: Q, 288 columns (2 bf16 per column)
 constexpr uint32_t kSCol = 320;    // rank 1: Cfg::kSBufs S buffers of N columns (up to column 512)
 constexpr uint32_t kTmemCols = 512;
 
-// P.V: A = P (K-major), B = V (MN-major); bf16, or f16 in the FP8 f16 mode
+// Modes: 0 bf16 cache (TMA), 3 sparse over the bf16 cache; quantised caches
+// (raw rings + dequant warps), exact bf16 operands / f16 operands: FP8
+// 594-byte row 1 / 2, FP4 324-byte row 4 / 5, FP8 528-byte V4.1 row 6 / 7.
+template <int kMode> constexpr bool kModeF16 = kMode == 2 || kMode == 5 || kMode == 7;
+template <int kMode> constexpr bool kModeQuant = kMode == 1 || kMode == 2 || kMode == 4 || kMode == 5 ||
+                                                 kMode == 6 || kMode == 7;
+template <int kMode> constexpr bool kModeV41 = kMode == 6 || kMode == 7;
+
+// P.V: A = P (K-major), B = V (MN-major); bf16, or f16 in the f16 modes
 template <int kMode>
-constexpr uint32_t kIdescPV =
-    (kMode == 2 || kMode == 5) ? ptx::idesc_f16(128, 256, 0, 1) : ptx::idesc_bf16(128, 256, 0, 1);
+constexpr uint32_t kIdescPV = kModeF16<kMode> ? ptx::idesc_f16(128, 256, 0, 1) : ptx::idesc_bf16(128, 256, 0, 1);
 
 constexpr float kLn2 = 0.69314718055994530942f;
 // log2 units: P <= 2^16 (exact in relative terms; O stays far from fp32
 // overflow).  The FP8 f16 mode keeps P <= 2^15, inside the f16 range.
 template <int kMode>
-constexpr float kRescaleThreshold = (kMode == 2 || kMode == 5) ? 15.0f : 16.0f;
+constexpr float kRescaleThreshold = kModeF16<kMode> ? 15.0f : 16.0f;
 
 // FP8 f16 mode: a scale exponent e in [113, 134] makes every e4m3 code times
 // 2^(e-127) an exact f16 number (largest 448 * 2^7 = 57344 < 65504; smallest
@@ -322,7 +333,9 @@ __device__ __forceinline__ bool dequant32_f16(const uint32_t* wd, uint32_t e, ui
 // Dequantise value group g (32 values) of raw FP8 row `row` (2-byte aligned
 // in shared memory) into 16 bf16x2 words.  The 32 codes are read as nine
 // aligned words and funnel-shifted by the row's misalignment (0 or 2 bytes).
-template <bool kF16 = false>
+// The group's e8m0 scale is byte kScales + g (576 for the 594-byte row, 512
+// for the 528-byte V4.1 row).
+template <bool kF16 = false, int kScales = kRow>
 __device__ __forceinline__ bool dequant_group(const uint8_t* row, int g, uint32_t* o) {
   const uint8_t* src = row + 32 * g;
   const uintptr_t a = reinterpret_cast<uintptr_t>(src);
@@ -334,9 +347,9 @@ __device__ __forceinline__ bool dequant_group(const uint8_t* row, int g, uint32_
 #pragma unroll
   for (int i = 0; i < 8; ++i) wd[i] = __funnelshift_r(u[i], u[i + 1], sh);
   if constexpr (kF16) {
-    return dequant32_f16(wd, row[kRow + g], o);
+    return dequant32_f16(wd, row[kScales + g], o);
   } else {
-    dequant32(wd, row[kRow + g], o);
+    dequant32(wd, row[kScales + g], o);
     return true;
   }
 }
@@ -432,17 +445,25 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float& qmax) {
 
 // With kF16 (FP8 f16 mode) the query is stored as f16, and qmax returns its
 // largest magnitude.
-template <int C0, int C1, bool kF16 = false>
+// kZero >= 0: that chunk is stored as zeros instead (the V4.1 row's latent
+// dims 448..511, which meet zero keys; a non-finite query value there would
+// otherwise turn its zero products into NaN).
+template <int C0, int C1, bool kF16 = false, int kZero = -1>
 __device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* qr, uint32_t taddr, float& qmax) {
   if constexpr (kF16) {
     // one chunk per round trip: the conversion needs the registers
 #pragma unroll 1
     for (int c = C0; c < C1; ++c) {
       uint32_t r0[32];
+      if (c == kZero) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v) ptx::ld_global_nc_v8((c < 8 ? qa + c * 128 : qr) + 32 * v, r0 + 8 * v);
+        for (int i = 0; i < 32; ++i) r0[i] = 0u;
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) r0[i] = bf16x2_to_f16x2(r0[i], qmax);
+        for (int v = 0; v < 4; ++v) ptx::ld_global_nc_v8((c < 8 ? qa + c * 128 : qr) + 32 * v, r0 + 8 * v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r0[i] = bf16x2_to_f16x2(r0[i], qmax);
+      }
       ptx::tmem_st32(taddr + 32u * c, r0);
     }
   } else {
@@ -455,6 +476,14 @@ __device__ __forceinline__ void load_q_chunks(const uint8_t* qa, const uint8_t* 
     if (two) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) ptx::ld_global_nc_v8((c + 1 < 8 ? qa + (c + 1) * 128 : qr) + 32 * v, r1 + 8 * v);
+    }
+    if (c == kZero) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r0[i] = 0u;
+    }
+    if (c + 1 == kZero) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r1[i] = 0u;
     }
     ptx::tmem_st32(taddr + 32u * c, r0);
     if (two) ptx::tmem_st32(taddr + 32u * (c + 1), r1);
@@ -495,13 +524,14 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
   constexpr int kVSlots = C::kVSlots;
   static_assert(C::kSBufs <= kMaxSBufs && kSCol + C::kSBufs * kN <= 512, "S buffers fit in TMEM");
   static_assert(C::kPSlots <= kMaxPSlots, "P slots and their alpha rows");
-  constexpr bool kQuant = kMode == 1 || kMode == 2 || kMode == 4 || kMode == 5;  // FP8 or FP4 cache (raw rings, dequant warps)
+  constexpr bool kQuant = kModeQuant<kMode>;   // FP8 or FP4 cache (raw rings, dequant warps)
   constexpr bool kFp4 = kMode == 4 || kMode == 5;
+  constexpr bool kV41 = kModeV41<kMode>;         // FP8 V4.1 row: 448 latent values, latent dims 448..511 zero
   // a quantised row and the half page the producer copies (its ring slots
   // are sized for the larger FP8 half page)
-  constexpr uint32_t kQRow = kFp4 ? kFp4Row : kFp8Row;
+  constexpr uint32_t kQRow = kFp4 ? kFp4Row : (kV41 ? kV41Row : kFp8Row);
   constexpr uint32_t kQRaw = kHalf * kQRow;
-  constexpr bool kF16 = kMode == 2 || kMode == 5;  // FP8 or FP4 with f16 operands
+  constexpr bool kF16 = kModeF16<kMode>;          // FP8 or FP4 with f16 operands
   constexpr uint32_t kIdescS =                    // A = Q (TMEM), B = K (K-major)
       kF16 ? ptx::idesc_f16(128, kN, 0, 0) : ptx::idesc_bf16(128, kN, 0, 0);
   constexpr uint32_t kOffAlpha = C::kOffMisc + kMiscAlpha;
@@ -879,6 +909,18 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
             } else if constexpr (kFp4) {
               dequant_group_fp4(row, g, o0);
               dequant_group_fp4(row + 16 * kQRow, g, o1);
+            } else if constexpr (kV41) {
+              // V4.1 row: groups 0..13 are the latent (dims 0..447), its
+              // groups 14 and 15 the RoPE values (this row's groups 16, 17);
+              // this row's groups 14 and 15 (dims 448..511) are zero
+              const int sg = g < 14 ? g : g - 2;
+              if (g == 14 || g == 15) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) { o0[e] = 0u; o1[e] = 0u; }
+              } else {
+                r0 = dequant_group<kF16, kV41Values>(row, sg, o0);
+                r1 = dequant_group<kF16, kV41Values>(row + 16 * kQRow, sg, o1);
+              }
             } else {
               r0 = dequant_group<kF16>(row, g, o0);
               r1 = dequant_group<kF16>(row + 16 * kQRow, g, o1);
@@ -1119,7 +1161,7 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
         const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope + (static_cast<size_t>(row) * kHeads + h) * kDr);
         const uint32_t qaddr = tmem + lane_base + kQCol;
         float qmax = 0.f;
-        if (kSG == 1) load_q_chunks<0, 9, kF16>(qa, qr, qaddr, qmax);
+        if (kSG == 1) load_q_chunks<0, 9, kF16, kV41 ? 7 : -1>(qa, qr, qaddr, qmax);
         else load_q_rolled(qa, qr, qaddr, grp == 0 ? 0 : 5, grp == 0 ? 5 : 9);
         if (kF16 && __any_sync(0xffffffffu, qmax > kF16Max) && lane == 0) atomicExch(&hdr->fp8_range, 1);
         ptx::tmem_wait_st();
@@ -1447,6 +1489,19 @@ cudaError_t launch_decode_fp4(const DecodeParams& p, int n_pairs, bool pdl, cuda
   if (e != cudaSuccess) return e;
   q.fp8_fallback = 1;
   return launch_decode_mode<4>(unused, q, n_pairs, pdl, stream);
+}
+
+cudaError_t launch_decode_fp8_v41(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
+  CacheMaps unused;
+  memset(&unused, 0, sizeof(unused));
+  // as for FP8: the f16-operand pass, then the exact bf16-operand pass,
+  // which returns at once unless the first pass flagged an input
+  DecodeParams q = p;
+  q.fp8_fallback = 0;
+  cudaError_t e = launch_decode_mode<7>(unused, q, n_pairs, pdl, stream);
+  if (e != cudaSuccess) return e;
+  q.fp8_fallback = 1;
+  return launch_decode_mode<6>(unused, q, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {

@@ -237,7 +237,10 @@ def workload_counts(inp: DecodeInputs) -> dict:
     out_bytes = inp.batch * sq * H * D_LATENT * 2
     lse_bytes = inp.batch * sq * H * 4
     bytes_ = kv_tokens * row_bytes + q_bytes + out_bytes + lse_bytes + used_pages * 4 + inp.batch * 4
-    flops = pairs * 2 * H * (ROW_ELEMS + D_LATENT)
+    # the V4.1 row carries a 448-value latent: the method's work is scores
+    # over 448 + 64 values and P.V over 448 (this path pads both to 512)
+    latent = V41_VALUES - D_ROPE if inp.kv_dtype == "fp8v41" else D_LATENT
+    flops = pairs * 2 * H * ((latent + D_ROPE) + latent)
     return dict(kv_tokens=kv_tokens, query_token_pairs=pairs, bytes=bytes_,
                 flops=flops, kv_bytes=kv_tokens * row_bytes)
 

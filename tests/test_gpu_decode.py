@@ -29,7 +29,8 @@ def to_dev(inp, dev="cuda"):
 def run_gpu(inp, d=None):
     d = d or to_dev(inp)
     ws = binding.alloc_workspace(inp.batch, inp.sq)
-    fn = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8, "fp4": binding.mla_decode_fp4}[inp.kv_dtype]
+    fn = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8, "fp4": binding.mla_decode_fp4,
+          "fp8v41": binding.mla_decode_fp8_v41}[inp.kv_dtype]
     out, lse = fn(d["q"], d["qr"], d["kv"], d["bt"], d["sl"], inp.scale, workspace=ws)
     st = binding.mla_get_status(ws)
     return out, lse, st
@@ -368,6 +369,73 @@ def test_fp8_query_beyond_f16_range_takes_the_exact_pass(cuda_device):
     assert st == 0
     assert torch.isfinite(out.float()).all()
     assert_close(out, lse, *oracle(inp))
+
+
+# ----------------------------------------------------------------- FP8 cache, V4.1 528-byte rows
+def _dequant_v41_bf16(raw: torch.Tensor) -> torch.Tensor:
+    """Oracle dequantisation of [..., 528] rows onto the 576-value row, cast
+    to bf16 (exact)."""
+    from oracle import fp8_codec
+    return torch.from_numpy(fp8_codec.dequant_rows_v41(raw.numpy())).to(torch.bfloat16)
+
+
+def test_fp8v41_single_token_is_bit_exact_dequant(cuda_device):
+    # scale bytes far outside the f16-exact range: the exact bf16 pass
+    inp = gen.make_inputs(8, 1, [1] * 8, kv_dtype="fp8v41", seed=32)
+    scales = [10, 11, 100, 120, 127, 130, 142, 143, 150, 200]
+    for b in range(8):
+        page = int(inp.block_table[b, 0])
+        row = inp.kv_cache[page, 0]
+        row[512:] = torch.tensor([scales[(b + k) % len(scales)] for k in range(16)], dtype=torch.uint8)
+        row[:8] = torch.tensor([0x00, 0x80, 0x01, 0x81, 0x7E, 0xFE, 0x08, 0x77], dtype=torch.uint8)
+        row[440:448] = torch.tensor([0x7E, 0xFE, 0x01, 0x81, 0x38, 0xB8, 0x08, 0x77], dtype=torch.uint8)
+    inp.q_absorbed[..., 448:] = float("nan")    # ignored: those latent dims are zero
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(8):
+        page = int(inp.block_table[b, 0])
+        want = _dequant_v41_bf16(inp.kv_cache[page, 0])[:512]
+        assert not want[448:].float().any()
+        got = out[b, 0].cpu()
+        assert torch.equal(got, want.expand(128, 512)), b   # value-exact (-0 == +0)
+
+
+def test_fp8v41_every_token_position_is_bit_exact_dequant(cuda_device):
+    # as for the 594-byte row: only the first RoPE dimension of the query is
+    # set, and token b's first RoPE value (byte 448 of the V4.1 row, scale
+    # byte 526) is +448 against -448 for every other token; the default
+    # scales (120..130) take the f16-operand pass
+    n = 64
+    inp = gen.make_inputs(n, 1, [n] * n, kv_dtype="fp8v41", seed=34)
+    inp.q_absorbed.zero_()
+    inp.q_rope.zero_()
+    inp.q_rope[..., 0] = 64.0
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        rows = inp.kv_cache[page]
+        rows[:, 448:512] = 0                 # RoPE codes: zero ...
+        rows[:, 512 + 14] = 127              # ... with scale 1 on the first RoPE group
+        rows[:, 448] = 0xFE                  # -448 for every token
+        rows[b, 448] = 0x7E                  # +448 for token b
+        rows[b, :8] = torch.tensor([0x00, 0x80, 0x01, 0x81, 0x7E, 0xFE, 0x08, 0x77], dtype=torch.uint8)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        want = _dequant_v41_bf16(inp.kv_cache[page, b])[:512]
+        got = out[b, 0].cpu()
+        assert torch.equal(got, want.expand(128, 512)), b
+
+
+@pytest.mark.parametrize("sq,lens", [(1, [1, 63, 64, 65, 200]), (1, [3000, 17]), (2, [70, 130, 1])])
+def test_fp8v41_ragged_and_causal(cuda_device, sq, lens):
+    inp = gen.make_inputs(len(lens), sq, lens, kv_dtype="fp8v41", seed=9 + len(lens) + sq)
+    ref = oracle(inp)
+    inp.q_absorbed[..., 448:] = float("nan")    # ignored: the oracle saw them as they were (finite)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *ref)
+    assert not out[..., 448:].float().any()
 
 
 def test_fp8_bad_page_sets_status(cuda_device):
