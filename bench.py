@@ -11,7 +11,7 @@ stream), an end-to-end number through the public API with host buffers, the
 float64 oracle timed on the host cores on a bounded sample, and the SM
 clocks sampled during the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..7]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..8]
   (workloads 1..5: the dense configurations; 6: sparse top-2048 decode;
   7: the FP4 cache at the FP8 workload's shape)
   python bench.py --impl reference ...   # the oracle arm (host cores)
