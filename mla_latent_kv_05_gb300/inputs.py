@@ -33,12 +33,14 @@ FP4_ROW_BYTES = ROW_ELEMS // 2 + FP4_NUM_SCALES # 324
 V41_VALUES = 512                                # V4.1 row: 448 latent + 64 RoPE values
 V41_NUM_SCALES = V41_VALUES // FP8_SCALE_GROUP  # 16
 V41_ROW_BYTES = V41_VALUES + V41_NUM_SCALES     # 528
+V41_FP4_ROW_BYTES = V41_VALUES // 2 + V41_VALUES // FP4_SCALE_GROUP   # 288
 DEFAULT_SCALE = 1.0 / math.sqrt(128 + 64)       # 1/sqrt(d_h + d_h^R)
 
 
 def row_bytes_of(kv_dtype: str) -> int:
     """Bytes of one cached token row in each cache format."""
-    return {"bf16": ROW_ELEMS * 2, "fp8": FP8_ROW_BYTES, "fp4": FP4_ROW_BYTES, "fp8v41": V41_ROW_BYTES}[kv_dtype]
+    return {"bf16": ROW_ELEMS * 2, "fp8": FP8_ROW_BYTES, "fp4": FP4_ROW_BYTES, "fp8v41": V41_ROW_BYTES,
+            "fp4v41": V41_FP4_ROW_BYTES}[kv_dtype]
 
 
 @dataclass
@@ -46,11 +48,12 @@ class DecodeInputs:
     """One decode call's inputs, on the host (CPU tensors)."""
     q_absorbed: torch.Tensor   # [B, Sq, H, 512] bf16
     q_rope: torch.Tensor       # [B, Sq, H, 64] bf16
-    kv_cache: torch.Tensor     # bf16 [P, 64, 576], uint8 [P, 64, 594] (fp8), [P, 64, 528] (fp8v41) or [P, 64, 324] (fp4)
+    kv_cache: torch.Tensor     # bf16 [P, 64, 576]; uint8 [P, 64, 594] (fp8), [P, 64, 528] (fp8v41),
+                               # [P, 64, 324] (fp4) or [P, 64, 288] (fp4v41)
     block_table: torch.Tensor  # int32 [B, max_pages], -1 where unused
     seq_lens: torch.Tensor     # int32 [B]
     scale: float
-    kv_dtype: str              # "bf16", "fp8", "fp8v41" or "fp4"
+    kv_dtype: str              # "bf16", "fp8", "fp8v41", "fp4" or "fp4v41"
     name: str = ""
     meta: dict = field(default_factory=dict)
 
@@ -88,6 +91,8 @@ WORKLOADS = {
             kv_dtype="fp4"),
     8: dict(name="fp8 V4.1 row B128 seq8192", batch=128, sq=1, seq=8192,
             kv_dtype="fp8v41"),
+    9: dict(name="fp4 V4.1 row B128 seq8192", batch=128, sq=1, seq=8192,
+            kv_dtype="fp4v41"),
 }
 
 
@@ -136,6 +141,22 @@ def _fp8v41_cache(gen: torch.Generator, num_pages: int, page_size: int) -> torch
         out[p0:p1, :, V41_VALUES:] = torch.randint(
             120, 131, (p1 - p0, page_size, V41_NUM_SCALES), generator=gen,
             dtype=torch.int64).to(torch.uint8)
+    return out
+
+
+def _fp4v41_cache(gen: torch.Generator, num_pages: int, page_size: int) -> torch.Tensor:
+    """[P, page, 288] uint8 V4.1 FP4 rows: 256 uniform random bytes (512
+    e2m1 codes, two per byte; 448 latent then 64 RoPE values) followed by 32
+    e8m0 exponent bytes drawn uniformly from [120, 130]."""
+    out = torch.empty((num_pages, page_size, V41_FP4_ROW_BYTES), dtype=torch.uint8)
+    step = 1024
+    nc = V41_VALUES // 2
+    for p0 in range(0, num_pages, step):
+        p1 = min(num_pages, p0 + step)
+        out[p0:p1, :, :nc] = torch.randint(0, 256, (p1 - p0, page_size, nc), generator=gen,
+                                           dtype=torch.int64).to(torch.uint8)
+        out[p0:p1, :, nc:] = torch.randint(120, 131, (p1 - p0, page_size, V41_VALUES // FP4_SCALE_GROUP),
+                                           generator=gen, dtype=torch.int64).to(torch.uint8)
     return out
 
 
@@ -192,6 +213,8 @@ def make_inputs(batch: int, sq: int, seq_lens, kv_dtype: str = "bf16",
         cache = _fp4_cache(gen, n_phys, page_size)
     elif kv_dtype == "fp8v41":
         cache = _fp8v41_cache(gen, n_phys, page_size)
+    elif kv_dtype == "fp4v41":
+        cache = _fp4v41_cache(gen, n_phys, page_size)
     else:
         raise ValueError(kv_dtype)
     return DecodeInputs(q_absorbed=q_abs, q_rope=q_rope, kv_cache=cache,
@@ -239,7 +262,7 @@ def workload_counts(inp: DecodeInputs) -> dict:
     bytes_ = kv_tokens * row_bytes + q_bytes + out_bytes + lse_bytes + used_pages * 4 + inp.batch * 4
     # the V4.1 row carries a 448-value latent: the method's work is scores
     # over 448 + 64 values and P.V over 448 (this path pads both to 512)
-    latent = V41_VALUES - D_ROPE if inp.kv_dtype == "fp8v41" else D_LATENT
+    latent = V41_VALUES - D_ROPE if inp.kv_dtype in ("fp8v41", "fp4v41") else D_LATENT
     flops = pairs * 2 * H * ((latent + D_ROPE) + latent)
     return dict(kv_tokens=kv_tokens, query_token_pairs=pairs, bytes=bytes_,
                 flops=flops, kv_bytes=kv_tokens * row_bytes)

@@ -18,6 +18,12 @@ followed by one e8m0 scale per 16 values.  That is 256 + 32 = 288 bytes for
 512 values, the record's figure, and 288 + 36 = 324 bytes for the 576-value
 row (512 latent, then 64 RoPE) decoded here: bytes [0, 288) hold the codes,
 bytes [288, 324) the 36 scales, scale k covering values [16k, 16k+16).
+
+The record's own 288-byte row (the V4.1 geometry, 512 values) is read the
+same way: bytes [0, 256) hold the 512 codes, bytes [256, 288) the 32 scales,
+and its 512 values are 448 latent values followed by the 64 RoPE values, as
+for the 528-byte FP8 row; on the 576-value row the latent fills dims
+[0, 448) and dims [448, 512) are zero.
 """
 from __future__ import annotations
 
@@ -30,6 +36,11 @@ SCALE_GROUP = 16
 NUM_SCALES = ROW_VALUES // SCALE_GROUP        # 36
 CODE_BYTES = ROW_VALUES // 2                  # 288
 ROW_BYTES = CODE_BYTES + NUM_SCALES           # 324
+
+V41_VALUES = 512                              # 448 latent + 64 RoPE
+V41_LATENT = 448
+V41_CODE_BYTES = V41_VALUES // 2              # 256
+V41_ROW_BYTES = V41_CODE_BYTES + V41_VALUES // SCALE_GROUP   # 288
 
 
 def e2m1_to_float64(codes: np.ndarray) -> np.ndarray:
@@ -64,3 +75,19 @@ def dequant_rows(raw: np.ndarray) -> np.ndarray:
     vals = e2m1_to_float64(unpack_codes(raw[..., :CODE_BYTES]))
     scales = e8m0_to_float64(raw[..., CODE_BYTES:])
     return vals * np.repeat(scales, SCALE_GROUP, axis=-1)
+
+
+def dequant_rows_v41(raw: np.ndarray) -> np.ndarray:
+    """[..., 288] uint8 V4.1 rows -> [..., 576] float64 values on this path's
+    row: dims [0, 448) the V4.1 latent, [448, 512) zero, [512, 576) the RoPE
+    values.  value[k] = e2m1(code k) * e8m0(byte[256 + k // 16])."""
+    raw = np.asarray(raw, dtype=np.uint8)
+    assert raw.shape[-1] == V41_ROW_BYTES, raw.shape
+    vals = e2m1_to_float64(unpack_codes(raw[..., :V41_CODE_BYTES]))
+    scales = e8m0_to_float64(raw[..., V41_CODE_BYTES:])
+    v = vals * np.repeat(scales, SCALE_GROUP, axis=-1)
+    out = np.zeros(raw.shape[:-1] + (ROW_VALUES,), dtype=np.float64)
+    out[..., :V41_LATENT] = v[..., :V41_LATENT]
+    out[..., ROW_VALUES - (V41_VALUES - V41_LATENT):] = v[..., V41_LATENT:]
+    return out
+

@@ -48,13 +48,15 @@ def visible_len(seq_len: int, sq: int, i: int) -> int:
 def cache_rows(kv_cache: np.ndarray, kv_dtype: str) -> np.ndarray:
     """The cache as float64 rows [P, page, 576]: bf16 caches arrive already
     widened to float64 by the caller; FP8 (594- and 528-byte rows) and FP4
-    caches are decoded here."""
+    (324- and 288-byte rows) caches are decoded here."""
     if kv_dtype == "fp8":
         return dequant_rows(kv_cache)
     if kv_dtype == "fp8v41":
         return dequant_rows_v41(kv_cache)
     if kv_dtype == "fp4":
         return fp4_codec.dequant_rows(kv_cache)
+    if kv_dtype == "fp4v41":
+        return fp4_codec.dequant_rows_v41(kv_cache)
     arr = np.asarray(kv_cache, dtype=np.float64)
     assert arr.shape[-1] == ROW
     return arr

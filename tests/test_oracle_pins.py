@@ -136,6 +136,39 @@ def test_v41_rows_equal_the_594_byte_rows_they_embed_in():
     assert not got[..., 448:512].any()
 
 
+def test_fp4_v41_row_is_the_printed_288_bytes():
+    # the record's FP4 variant: 288 bytes per token for the 512-value row
+    assert cf.fp4_row_bytes(512) == 288 == fp4_codec.V41_ROW_BYTES
+
+
+def test_fp4_v41_row_layout_by_hand():
+    # code bytes 0x22 (both nibbles 1.0), scale of group k (16 values) =
+    # 2^(k - 10): value k of the row is 2^(k//16 - 10); latent values in dims
+    # [0, 448), RoPE values (the row's last 64) in [512, 576), zeros between
+    row = np.zeros(288, dtype=np.uint8)
+    row[:256] = 0x22
+    row[256:] = 117 + np.arange(32)
+    got = fp4_codec.dequant_rows_v41(row)
+    v = 2.0 ** (np.arange(512) // 16 - 10)
+    want = np.zeros(576)
+    want[:448] = v[:448]
+    want[512:] = v[448:]
+    assert np.array_equal(got, want)
+    assert got[447] == 2.0 ** 17 and not got[448:512].any() and got[512] == 2.0 ** 18 and got[575] == 2.0 ** 21
+
+
+def test_fp4_v41_rows_equal_the_324_byte_rows_they_embed_in():
+    inp = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp4v41", seed=6)
+    raw = inp.kv_cache.numpy()
+    wide = np.zeros(raw.shape[:-1] + (324,), dtype=np.uint8)
+    wide[..., :224] = raw[..., :224]                 # latent codes (values 0..447)
+    wide[..., 256:288] = raw[..., 224:256]           # RoPE codes (values 512..575)
+    wide[..., 288:316] = raw[..., 256:284]           # latent scales (groups 0..27)
+    wide[..., 316:320] = 127                         # groups 28..31: zero codes, any scale
+    wide[..., 320:324] = raw[..., 284:288]           # RoPE scales
+    assert np.array_equal(fp4_codec.dequant_rows_v41(raw), fp4_codec.dequant_rows(wide))
+
+
 def test_e2m1_table_is_the_ocp_value_set():
     # OCP MX FP4 E2M1: the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 in
     # code order, the sign bit negating them; no NaN or infinity
