@@ -11,7 +11,7 @@ stream), an end-to-end number through the public API with host buffers, the
 float64 oracle timed on the host cores on a bounded sample, and the SM
 clocks sampled during the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..8]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..9]
   (workloads 1..5: the dense configurations; 6: sparse top-2048 decode;
   7: the FP4 cache at the FP8 workload's shape)
   python bench.py --impl reference ...   # the oracle arm (host cores)
@@ -351,7 +351,8 @@ def run_ours(args):
     else:
         counts = gen.workload_counts(inp)
         decode = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8,
-                  "fp4": binding.mla_decode_fp4, "fp8v41": binding.mla_decode_fp8_v41}[inp.kv_dtype]
+                  "fp4": binding.mla_decode_fp4, "fp8v41": binding.mla_decode_fp8_v41,
+                  "fp4v41": binding.mla_decode_fp4_v41}[inp.kv_dtype]
         bt = inp.block_table.to(dev)
         sl = inp.seq_lens.to(dev)
         ws = binding.alloc_workspace(inp.batch, inp.sq, dev)

@@ -196,6 +196,22 @@ int mla_decode_fp8_v41(const uint16_t* q_absorbed, const uint16_t* q_rope,
                        float softmax_scale, uint16_t* out, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Same over an FP4 cache in the record's own 288-byte row [num_pages, 64,
+ * 288] (uint8; the FP4 variant of the V4.1 row, 512 values): 256 bytes of
+ * e2m1 codes (two per byte, value 2k in the low nibble of byte k), then 32
+ * e8m0 scales, one per 16 values:
+ *   v[k] = e2m1(nibble k) * 2^(byte[256 + k/16] - 127),
+ * latent = v[0..447], RoPE key = v[448..511], as for mla_decode_fp8_v41
+ * (query dims 448..511 ignored, output dims 448..511 written as 0).
+ * Exactness and the f16-operand pass are those of mla_decode_fp4;
+ * kv_cache must be 16-byte aligned. */
+int mla_decode_fp4_v41(const uint16_t* q_absorbed, const uint16_t* q_rope,
+                       const uint8_t* kv_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, int batch, int sq, int num_heads,
+                       int num_pages, int page_size, int max_pages,
+                       float softmax_scale, uint16_t* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Sparse top-k decode ("DeepSeek-V3.2" model record: the sparse attention
  * indexer, index_topk 2048, selects the candidate tokens each query attends
  * over; the latent rows stay cached per token).  Query row (b, i) attends

@@ -36,6 +36,8 @@ SIGNATURES = {
                             ctypes.c_size_t, _P]),
     "mla_decode_fp8_v41": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                                 ctypes.c_size_t, _P]),
+    "mla_decode_fp4_v41": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                                ctypes.c_size_t, _P]),
     "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_decode_sparse_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
@@ -219,6 +221,16 @@ def mla_decode_fp8_v41(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scal
     ignored)."""
     return _decode("mla_decode_fp8_v41", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
                    workspace, stream, torch.uint8, 528)
+
+
+def mla_decode_fp4_v41(q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out=None, lse=None,
+                       workspace=None, stream=None):
+    """MLA decode over an FP4 latent cache in the 288-byte V4.1 row layout
+    [num_pages, 64, 288] (uint8 rows: 512 e2m1 codes, two per byte, 448
+    latent then 64 RoPE values, then 32 e8m0 scales, one per 16 values);
+    returns (out, lse) as mla_decode_fp8_v41 does."""
+    return _decode("mla_decode_fp4_v41", q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale, out, lse,
+                   workspace, stream, torch.uint8, 288)
 
 
 def mla_workspace_size_sparse(batch: int, sq: int, topk: int, num_heads: int = 128, page_size: int = 64) -> int:

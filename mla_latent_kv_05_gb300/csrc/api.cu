@@ -71,7 +71,7 @@ int validate_common(const void* q_absorbed, const void* q_rope, const void* kv_c
   return MLA_OK;
 }
 
-enum class CacheKind { kBf16, kFp8, kFp4, kFp8V41 };
+enum class CacheKind { kBf16, kFp8, kFp4, kFp8V41, kFp4V41 };
 
 // CTA pairs a query index gets: all resident pairs, but no more than one per
 // kPagesPerPair pages the call can hold (batch * max_pages, known on the host
@@ -147,6 +147,7 @@ int run_decode(CacheKind kind, const uint16_t* q_absorbed, const uint16_t* q_rop
   if (kind == CacheKind::kFp8) le = launch_decode_fp8(p, ppg * sq, pdl, stream);
   else if (kind == CacheKind::kFp4) le = launch_decode_fp4(p, ppg * sq, pdl, stream);
   else if (kind == CacheKind::kFp8V41) le = launch_decode_fp8_v41(p, ppg * sq, pdl, stream);
+  else if (kind == CacheKind::kFp4V41) le = launch_decode_fp4_v41(p, ppg * sq, pdl, stream);
   else le = launch_decode_bf16(maps, p, ppg * sq, pdl, stream);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -356,6 +357,14 @@ int mla_decode_fp8_v41(const uint16_t* q_absorbed, const uint16_t* q_rope, const
                        int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream) {
   return run_decode(CacheKind::kFp8V41, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads,
+                    num_pages, page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_fp4_v41(const uint16_t* q_absorbed, const uint16_t* q_rope, const uint8_t* kv_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, int batch, int sq, int num_heads,
+                       int num_pages, int page_size, int max_pages, float softmax_scale, uint16_t* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  return run_decode(CacheKind::kFp4V41, q_absorbed, q_rope, kv_cache, block_table, seq_lens, batch, sq, num_heads,
                     num_pages, page_size, max_pages, softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 

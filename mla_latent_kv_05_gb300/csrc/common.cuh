@@ -25,6 +25,9 @@ constexpr int kFp4Row = kFp4Codes + kRow / 16;   // ... then 36 e8m0 scales (one
 constexpr int kV41Values = 512;
 constexpr int kV41Latent = 448;
 constexpr int kV41Row = kV41Values + kV41Values / 32;   // 528 bytes
+// FP4 V4.1 row: 512 e2m1 codes (two per byte), then 32 e8m0 scales (one per
+// 16 values): 288 bytes, the same value order.
+constexpr int kV41Fp4Row = kV41Values / 2 + kV41Values / 16;   // 288 bytes
 constexpr int kMaxSq = 4;
 constexpr int kMaxRows = 1 << 16;   // batch * Sq handled by the planner
 

@@ -148,6 +148,9 @@ template <> struct Cfg<5> : Cfg<1> {};
 // operands (exact), 7 = f16 operands
 template <> struct Cfg<6> : Cfg<1> {};
 template <> struct Cfg<7> : Cfg<1> {};
+// FP4 V4.1 cache (288-byte rows): 8 = bf16 operands (exact), 9 = f16 operands
+template <> struct Cfg<8> : Cfg<1> {};
+template <> struct Cfg<9> : Cfg<1> {};
 // sparse decode over the bf16 cache: the bf16 plan, K and V gathered by rows
 template <> struct Cfg<3> : Cfg<0> {};
 constexpr int kGatherWarps = 3;          // sparse: warps 0, 2, 3 of each rank copy one half page of a tile each
@@ -186,11 +189,12 @@ constexpr uint32_t kTmemCols = 512;
 
 // Modes: 0 bf16 cache (TMA), 3 sparse over the bf16 cache; quantised caches
 // (raw rings + dequant warps), exact bf16 operands / f16 operands: FP8
-// 594-byte row 1 / 2, FP4 324-byte row 4 / 5, FP8 528-byte V4.1 row 6 / 7.
-template <int kMode> constexpr bool kModeF16 = kMode == 2 || kMode == 5 || kMode == 7;
-template <int kMode> constexpr bool kModeQuant = kMode == 1 || kMode == 2 || kMode == 4 || kMode == 5 ||
-                                                 kMode == 6 || kMode == 7;
-template <int kMode> constexpr bool kModeV41 = kMode == 6 || kMode == 7;
+// 594-byte row 1 / 2, FP4 324-byte row 4 / 5, FP8 528-byte V4.1 row 6 / 7,
+// FP4 288-byte V4.1 row 8 / 9.
+template <int kMode> constexpr bool kModeF16 = kMode == 2 || kMode == 5 || kMode == 7 || kMode == 9;
+template <int kMode> constexpr bool kModeQuant = kMode == 1 || kMode == 2 || (kMode >= 4 && kMode <= 9);
+template <int kMode> constexpr bool kModeFp4 = kMode == 4 || kMode == 5 || kMode == 8 || kMode == 9;
+template <int kMode> constexpr bool kModeV41 = kMode >= 6 && kMode <= 9;
 
 // P.V: A = P (K-major), B = V (MN-major); bf16, or f16 in the f16 modes
 template <int kMode>
@@ -367,9 +371,12 @@ __device__ __forceinline__ float e8m0_f32(uint32_t e) {
   return __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : (e << 23)));
 }
 
+// kScales: the first scale byte (288 for the 324-byte row, 256 for the
+// 288-byte V4.1 row).
+template <int kScales = kFp4Codes>
 __device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uint32_t* o) {
   const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 16 * g);
-  const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + kFp4Codes + 2 * g);
+  const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + kScales + 2 * g);
   const float s0 = e8m0_f32(sc & 0xFFu), s1 = e8m0_f32(sc >> 8);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -396,9 +403,10 @@ __device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uin
 // normal f16 number.  Returns false for a scale outside that range.
 constexpr uint32_t kFp4F16ScaleLo = 113, kFp4F16ScaleHi = 140;
 
+template <int kScales = kFp4Codes>
 __device__ __forceinline__ bool dequant_group_fp4_f16(const uint8_t* row, int g, uint32_t* o) {
   const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 16 * g);
-  const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + kFp4Codes + 2 * g);
+  const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + kScales + 2 * g);
   const uint32_t e0 = sc & 0xFFu, e1 = sc >> 8;
   const bool in_range = e0 >= kFp4F16ScaleLo && e0 <= kFp4F16ScaleHi && e1 >= kFp4F16ScaleLo && e1 <= kFp4F16ScaleHi;
   const uint32_t f0 = ((e0 - 112u) & 31u) << 10, f1 = ((e1 - 112u) & 31u) << 10;
@@ -525,11 +533,11 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
   static_assert(C::kSBufs <= kMaxSBufs && kSCol + C::kSBufs * kN <= 512, "S buffers fit in TMEM");
   static_assert(C::kPSlots <= kMaxPSlots, "P slots and their alpha rows");
   constexpr bool kQuant = kModeQuant<kMode>;   // FP8 or FP4 cache (raw rings, dequant warps)
-  constexpr bool kFp4 = kMode == 4 || kMode == 5;
-  constexpr bool kV41 = kModeV41<kMode>;         // FP8 V4.1 row: 448 latent values, latent dims 448..511 zero
+  constexpr bool kFp4 = kModeFp4<kMode>;
+  constexpr bool kV41 = kModeV41<kMode>;         // V4.1 row: 448 latent values, latent dims 448..511 zero
   // a quantised row and the half page the producer copies (its ring slots
   // are sized for the larger FP8 half page)
-  constexpr uint32_t kQRow = kFp4 ? kFp4Row : (kV41 ? kV41Row : kFp8Row);
+  constexpr uint32_t kQRow = kFp4 ? (kV41 ? kV41Fp4Row : kFp4Row) : (kV41 ? kV41Row : kFp8Row);
   constexpr uint32_t kQRaw = kHalf * kQRow;
   constexpr bool kF16 = kModeF16<kMode>;          // FP8 or FP4 with f16 operands
   constexpr uint32_t kIdescS =                    // A = Q (TMEM), B = K (K-major)
@@ -903,24 +911,30 @@ mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParam
           if (raw_flag[rs] == 0) {
             const uint8_t* row = smem + raw_off + static_cast<uint32_t>(rs) * kRawBytes + t * kQRow;
             bool r0 = true, r1 = true;
-            if constexpr (kFp4 && kF16) {
-              r0 = dequant_group_fp4_f16(row, g, o0);
-              r1 = dequant_group_fp4_f16(row + 16 * kQRow, g, o1);
-            } else if constexpr (kFp4) {
-              dequant_group_fp4(row, g, o0);
-              dequant_group_fp4(row + 16 * kQRow, g, o1);
-            } else if constexpr (kV41) {
-              // V4.1 row: groups 0..13 are the latent (dims 0..447), its
+            if constexpr (kV41) {
+              // V4.1 row: its groups 0..13 are the latent (dims 0..447), its
               // groups 14 and 15 the RoPE values (this row's groups 16, 17);
               // this row's groups 14 and 15 (dims 448..511) are zero
               const int sg = g < 14 ? g : g - 2;
               if (g == 14 || g == 15) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) { o0[e] = 0u; o1[e] = 0u; }
+              } else if constexpr (kFp4 && kF16) {
+                r0 = dequant_group_fp4_f16<kV41Values / 2>(row, sg, o0);
+                r1 = dequant_group_fp4_f16<kV41Values / 2>(row + 16 * kQRow, sg, o1);
+              } else if constexpr (kFp4) {
+                dequant_group_fp4<kV41Values / 2>(row, sg, o0);
+                dequant_group_fp4<kV41Values / 2>(row + 16 * kQRow, sg, o1);
               } else {
                 r0 = dequant_group<kF16, kV41Values>(row, sg, o0);
                 r1 = dequant_group<kF16, kV41Values>(row + 16 * kQRow, sg, o1);
               }
+            } else if constexpr (kFp4 && kF16) {
+              r0 = dequant_group_fp4_f16(row, g, o0);
+              r1 = dequant_group_fp4_f16(row + 16 * kQRow, g, o1);
+            } else if constexpr (kFp4) {
+              dequant_group_fp4(row, g, o0);
+              dequant_group_fp4(row + 16 * kQRow, g, o1);
             } else {
               r0 = dequant_group<kF16>(row, g, o0);
               r1 = dequant_group<kF16>(row + 16 * kQRow, g, o1);
@@ -1502,6 +1516,17 @@ cudaError_t launch_decode_fp8_v41(const DecodeParams& p, int n_pairs, bool pdl, 
   if (e != cudaSuccess) return e;
   q.fp8_fallback = 1;
   return launch_decode_mode<6>(unused, q, n_pairs, pdl, stream);
+}
+
+cudaError_t launch_decode_fp4_v41(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {
+  CacheMaps unused;
+  memset(&unused, 0, sizeof(unused));
+  DecodeParams q = p;
+  q.fp8_fallback = 0;
+  cudaError_t e = launch_decode_mode<9>(unused, q, n_pairs, pdl, stream);
+  if (e != cudaSuccess) return e;
+  q.fp8_fallback = 1;
+  return launch_decode_mode<8>(unused, q, n_pairs, pdl, stream);
 }
 
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream) {

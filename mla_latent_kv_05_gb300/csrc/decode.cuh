@@ -48,6 +48,7 @@ cudaError_t launch_decode_bf16(const CacheMaps& maps, const DecodeParams& p, int
 cudaError_t launch_decode_fp8(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 cudaError_t launch_decode_fp4(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 cudaError_t launch_decode_fp8_v41(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
+cudaError_t launch_decode_fp4_v41(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);
 // Sparse decode over the bf16 cache (p.kv_bf16, p.sp_slots; rows planned
 // with one query each).
 cudaError_t launch_decode_sparse(const DecodeParams& p, int n_pairs, bool pdl, cudaStream_t stream);

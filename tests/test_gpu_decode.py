@@ -30,7 +30,7 @@ def run_gpu(inp, d=None):
     d = d or to_dev(inp)
     ws = binding.alloc_workspace(inp.batch, inp.sq)
     fn = {"bf16": binding.mla_decode_bf16, "fp8": binding.mla_decode_fp8, "fp4": binding.mla_decode_fp4,
-          "fp8v41": binding.mla_decode_fp8_v41}[inp.kv_dtype]
+          "fp8v41": binding.mla_decode_fp8_v41, "fp4v41": binding.mla_decode_fp4_v41}[inp.kv_dtype]
     out, lse = fn(d["q"], d["qr"], d["kv"], d["bt"], d["sl"], inp.scale, workspace=ws)
     st = binding.mla_get_status(ws)
     return out, lse, st
@@ -517,6 +517,51 @@ def test_fp4_scale_at_the_f16_range_edges(cuda_device, scale_byte):
     assert st == 0
     assert torch.isfinite(out.float()).all()
     assert_close(out, lse, *oracle(inp))
+
+
+# FP4 V4.1 rows: 256 code bytes (512 values: 448 latent, then 64 RoPE), then
+# 32 e8m0 scales, one per 16 values.
+
+def test_fp4v41_every_token_position_is_bit_exact_dequant(cuda_device):
+    # as for the 324-byte row: token b's first RoPE value (code byte 224, low
+    # nibble; scale byte 256 + 28) is +6 * 2^4 against -6 * 2^4 elsewhere;
+    # token b's first code bytes cover all sixteen codes in both nibbles and
+    # its scales span a wide range (the exact bf16 pass)
+    n = 64
+    inp = gen.make_inputs(n, 1, [n] * n, kv_dtype="fp4v41", seed=36)
+    inp.q_absorbed.zero_()
+    inp.q_absorbed[..., 448:] = float("nan")   # ignored
+    inp.q_rope.zero_()
+    inp.q_rope[..., 0] = 16.0
+    scales = [2, 10, 100, 119, 127, 128, 135, 150, 200, 252]
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        rows = inp.kv_cache[page]
+        rows[:, 224:256] = 0                     # RoPE codes (values 448..511): zero ...
+        rows[:, 256 + 28] = 131                  # ... scale 2^4 on values 448..463
+        rows[:, 224] = 0x0F                      # RoPE value 0 = -6 * 2^4 for every token ...
+        rows[b, 224] = 0x07                      # ... and +6 * 2^4 for token b
+        rows[b, :16] = torch.tensor([0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE,
+                                     0x01, 0x23, 0x45, 0x67, 0x89, 0xAB, 0xCD, 0xEF], dtype=torch.uint8)
+        rows[b, 256:256 + 28] = torch.tensor([scales[(b + k) % len(scales)] for k in range(28)], dtype=torch.uint8)
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    for b in range(n):
+        page = int(inp.block_table[b, 0])
+        want = torch.from_numpy(fp4_codec.dequant_rows_v41(inp.kv_cache[page, b].numpy())).to(torch.bfloat16)[:512]
+        got = out[b, 0].cpu()
+        assert torch.equal(got, want.expand(128, 512)), b
+
+
+@pytest.mark.parametrize("sq,lens", [(1, [1, 63, 64, 65, 200]), (1, [3000, 17]), (2, [70, 5000, 130])])
+def test_fp4v41_ragged_and_causal(cuda_device, sq, lens):
+    inp = gen.make_inputs(len(lens), sq, lens, kv_dtype="fp4v41", seed=27 + len(lens) + sq)
+    ref = oracle(inp)
+    inp.q_absorbed[..., 448:] = float("nan")
+    out, lse, st = run_gpu(inp)
+    assert st == 0
+    assert_close(out, lse, *ref)
+    assert not out[..., 448:].float().any()
 
 
 def test_fp4_bad_page_sets_status(cuda_device):

@@ -21,7 +21,7 @@ def sampled_rows(inp, k=4):
     return [(b, i) for b in sorted(bs) for i in range(inp.sq)]
 
 
-@pytest.mark.parametrize("workload", [2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("workload", [2, 3, 4, 5, 7, 8, 9])
 def test_workload_full_size(cuda_device, workload):
     inp = gen.make_workload(workload)
     out, lse, st = run_gpu(inp)
