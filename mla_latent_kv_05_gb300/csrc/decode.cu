@@ -1442,8 +1442,9 @@ namespace {
 // Host-side launcher.  kMode 0: bf16 cache through the 4-D tensor maps
 // (half- and whole-page boxes of chunks 0..4 and 5..8 for rank 1, half-page
 // boxes of the eight latent chunks for rank 0); 1 and 2: FP8 cache, 4 and 5:
-// FP4 cache (p.kv_quant; tensor maps unused; 2 and 5 take f16 operands, 1
-// and 4 bf16); 3: sparse gather from the bf16 cache.  It lives in an
+// FP4 cache, 6 and 7: FP8 V4.1 rows, 8 and 9: FP4 V4.1 rows (p.kv_quant;
+// tensor maps unused; 2, 5, 7 and 9 take f16 operands, 1, 4, 6 and 8
+// bf16); 3: sparse gather from the bf16 cache.  It lives in an
 // unnamed namespace so that its per-device static is this library's own:
 // a function-local static of a template with external linkage is one
 // object per process, shared by every loaded copy of the library.
