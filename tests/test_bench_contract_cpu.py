@@ -20,7 +20,7 @@ def _run(*args):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("workload", ["1", "7"])
+@pytest.mark.parametrize("workload", ["1", "7", "9"])
 def test_reference_arm_prints_the_contract_line(workload):
     d = _run("--impl", "reference", "--workload", workload, "--steps", "3", "--warmup", "3")
     assert d["impl"] == "reference"
@@ -34,7 +34,7 @@ def test_reference_arm_prints_the_contract_line(workload):
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
-    kv = {"1": "bf16", "7": "fp4"}[workload]
+    kv = {"1": "bf16", "7": "fp4", "9": "fp4v41"}[workload]
     assert d["config"]["kv_dtype"] == kv
 
 
