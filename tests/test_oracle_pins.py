@@ -169,6 +169,48 @@ def test_fp4_v41_rows_equal_the_324_byte_rows_they_embed_in():
     assert np.array_equal(fp4_codec.dequant_rows_v41(raw), fp4_codec.dequant_rows(wide))
 
 
+def _v41_fp8_pins_ok(decode) -> bool:
+    """The 528-byte row's hand-built pin and its 594-byte embedding, for a
+    candidate decoder [..., 528] -> [..., 576]."""
+    row = np.zeros(528, dtype=np.uint8)
+    row[:512] = 0x38
+    row[512:] = 120 + np.arange(16)
+    v = 2.0 ** (np.arange(512) // 32 - 7)
+    want = np.zeros(576)
+    want[:448], want[512:] = v[:448], v[448:]
+    if not np.array_equal(decode(row), want):
+        return False
+    raw = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp8v41", seed=5).kv_cache.numpy()
+    wide = np.zeros(raw.shape[:-1] + (594,), dtype=np.uint8)
+    wide[..., :448], wide[..., 512:576] = raw[..., :448], raw[..., 448:512]
+    wide[..., 576:590], wide[..., 590:592], wide[..., 592:594] = raw[..., 512:526], 127, raw[..., 526:528]
+    return np.array_equal(decode(raw), fp8_codec.dequant_rows(wide))
+
+
+def test_v41_pins_catch_planted_mistakes():
+    good = fp8_codec.dequant_rows_v41
+    assert _v41_fp8_pins_ok(good)
+
+    def scales_one_group_late(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., 512:] = np.roll(raw[..., 512:], 1, axis=-1)
+        return good(raw)
+
+    def rope_in_the_padding(raw):
+        out = good(raw)
+        fixed = out.copy()
+        fixed[..., 448:512], fixed[..., 512:] = out[..., 512:], 0
+        return fixed
+
+    def padding_not_zero(raw):
+        out = good(raw)
+        out[..., 448:512] = out[..., 512:]
+        return out
+
+    for bad in (scales_one_group_late, rope_in_the_padding, padding_not_zero):
+        assert not _v41_fp8_pins_ok(bad), bad.__name__
+
+
 def test_e2m1_table_is_the_ocp_value_set():
     # OCP MX FP4 E2M1: the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 in
     # code order, the sign bit negating them; no NaN or infinity
