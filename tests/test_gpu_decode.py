@@ -564,6 +564,14 @@ def test_fp4v41_ragged_and_causal(cuda_device, sq, lens):
     assert not out[..., 448:].float().any()
 
 
+@pytest.mark.parametrize("kv", ["fp8v41", "fp4v41"])
+def test_v41_bad_page_sets_status(cuda_device, kv):
+    inp = gen.make_inputs(2, 1, [100, 64], kv_dtype=kv, seed=7)
+    inp.block_table[1, 0] = -3
+    _, _, st = run_gpu(inp)
+    assert st == -5
+
+
 def test_fp4_bad_page_sets_status(cuda_device):
     inp = gen.make_inputs(2, 1, [100, 64], kv_dtype="fp4", seed=5)
     inp.block_table[1, 0] = -3
