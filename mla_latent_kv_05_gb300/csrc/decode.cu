@@ -342,14 +342,22 @@ __device__ __forceinline__ bool dequant32_f16(const uint32_t* wd, uint32_t e, ui
 template <bool kF16 = false, int kScales = kRow>
 __device__ __forceinline__ bool dequant_group(const uint8_t* row, int g, uint32_t* o) {
   const uint8_t* src = row + 32 * g;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(src);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
-  const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
-  uint32_t u[9], wd[8];
+  uint32_t wd[8];
+  if constexpr (kScales == kV41Values) {
+    // 528-byte rows start on 16-byte boundaries: two 16-byte loads
+    const uint4 lo = *reinterpret_cast<const uint4*>(src), hi = *reinterpret_cast<const uint4*>(src + 16);
+    wd[0] = lo.x; wd[1] = lo.y; wd[2] = lo.z; wd[3] = lo.w;
+    wd[4] = hi.x; wd[5] = hi.y; wd[6] = hi.z; wd[7] = hi.w;
+  } else {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
+    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+    uint32_t u[9];
 #pragma unroll
-  for (int i = 0; i < 9; ++i) u[i] = w[i];
+    for (int i = 0; i < 9; ++i) u[i] = w[i];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) wd[i] = __funnelshift_r(u[i], u[i + 1], sh);
+    for (int i = 0; i < 8; ++i) wd[i] = __funnelshift_r(u[i], u[i + 1], sh);
+  }
   if constexpr (kF16) {
     return dequant32_f16(wd, row[kScales + g], o);
   } else {
