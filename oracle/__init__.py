@@ -17,9 +17,11 @@ Sources (web pages, cited by title and section):
   * "DeepSeek-V3.2" model record: the same cache figures.
 
 Modules:
-  fp8_codec     e4m3 (OCP E4M3FN) and e8m0 decoders, FP8 row dequantisation
+  fp8_codec     e4m3 (OCP E4M3FN) and e8m0 decoders, FP8 row dequantisation;
+                the e4m3 encoder and per-32 block quantiser of a query
   fp4_codec     e2m1 (OCP MX FP4) decoder, FP4 row dequantisation
-  mla_oracle    absorbed and un-absorbed attention, paged gather, LSE merge
+  mla_oracle    absorbed and un-absorbed attention, paged gather, LSE merge,
+                the query as two e4m3 terms
   closed_forms  the pages' cache-size arithmetic
 
 Every function here is pinned by a CPU test against something other than

@@ -84,3 +84,72 @@ def dequant_rows_v41(raw: np.ndarray) -> np.ndarray:
     out[..., ROW_VALUES - (V41_VALUES - V41_LATENT):] = v[..., V41_LATENT:]
     return out
 
+
+
+# ---------------------------------------------------------------------------
+# Encoding: the query side of a block-scaled FP8 score product.
+#
+# Reading taken (the record's constraint (2) fixes the cache's codes and
+# scales, not the query's): the query is quantised like a cache row, e4m3
+# codes with one e8m0 scale per 32 values, the scale being the smallest power
+# of two that brings the group's largest magnitude to at most 448 (the e4m3
+# maximum normal, architecture guide section 4), codes rounded to nearest with
+# ties to even.  One such term keeps four significant bits of each value; the
+# residual q - deq(hi), quantised the same way, gives a second term, and the
+# two together carry about as many bits as the bf16 query does.
+
+def float64_to_e4m3fn(x: np.ndarray) -> np.ndarray:
+    """Encode float64 values with |x| <= 448 as OCP E4M3FN bytes, rounding to
+    nearest, ties to even (the encoding's own grid: spacing 2^(e-3) in the
+    binade [2^e, 2^(e+1)) for e >= -6, spacing 2^-9 below 2^-6)."""
+    x = np.asarray(x, dtype=np.float64)
+    assert np.all(np.isfinite(x)) and np.all(np.abs(x) <= 448.0), "outside the e4m3 range"
+    a = np.abs(x)
+    _, ex = np.frexp(a)                             # a = m 2^ex, m in [0.5, 1)
+    e = np.maximum(ex.astype(np.int64) - 1, -6)     # binade exponent, floored at the subnormal range
+    quantum = np.exp2((e - 3).astype(np.float64))
+    n = np.rint(a / quantum)                        # numpy rounds half to even
+    v = n * quantum                                 # the rounded magnitude, exact
+    _, vex = np.frexp(v)
+    normal = v >= 2.0 ** -6
+    exp_field = np.where(normal, vex.astype(np.int64) - 1 + 7, 0)
+    man_field = np.where(normal, v / np.exp2((exp_field - 7).astype(np.float64)) * 8 - 8, v / 2.0 ** -9)
+    code = (exp_field << 3) | man_field.astype(np.int64)
+    return (code | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
+
+
+def block_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Smallest integer k with amax <= 448 * 2^k (k = 0 for an all-zero group).
+    With amax = m 2^E, m in [0.5, 1): 448 * 2^k = 0.875 * 2^(k+9), so k = E - 9
+    when m <= 0.875 and E - 8 otherwise, with no rounding anywhere."""
+    amax = np.asarray(amax, dtype=np.float64)
+    m, ex = np.frexp(amax)
+    k = np.where(m <= 0.875, ex - 9, ex - 8).astype(np.int64)
+    return np.where(amax == 0, 0, k)
+
+
+def quantise_blocks(x: np.ndarray, group: int = SCALE_GROUP):
+    """[..., n] float64 -> (e4m3 codes [..., n], e8m0 scale codes [..., n/group]).
+    Group g's scale is 2^k with k = block_scale_exponent(max |x| over the group);
+    its codes are e4m3(x / 2^k)."""
+    x = np.asarray(x, dtype=np.float64)
+    assert x.shape[-1] % group == 0
+    g = x.reshape(x.shape[:-1] + (x.shape[-1] // group, group))
+    k = block_scale_exponent(np.abs(g).max(axis=-1))
+    assert np.all((k >= -127) & (k <= 127)), "scale outside e8m0"
+    codes = float64_to_e4m3fn(g / np.exp2(k.astype(np.float64))[..., None])
+    return codes.reshape(x.shape), (k + 127).astype(np.uint8)
+
+
+def dequant_blocks(codes: np.ndarray, scales: np.ndarray, group: int = SCALE_GROUP) -> np.ndarray:
+    """The inverse map: value[k] = e4m3(codes[k]) * e8m0(scales[k // group])."""
+    return e4m3fn_to_float64(codes) * np.repeat(e8m0_to_float64(scales), group, axis=-1)
+
+
+def split_e4m3_terms(x: np.ndarray, group: int = SCALE_GROUP):
+    """x ~ hi + lo: hi = quantise_blocks(x), lo = quantise_blocks(x - deq(hi)).
+    Returns ((hi codes, hi scales), (lo codes, lo scales))."""
+    x = np.asarray(x, dtype=np.float64)
+    hi = quantise_blocks(x, group)
+    lo = quantise_blocks(x - dequant_blocks(*hi, group=group), group)
+    return hi, lo

@@ -32,7 +32,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fp8_codec import dequant_rows, dequant_rows_v41
+from .fp8_codec import dequant_blocks, dequant_rows, dequant_rows_v41, split_e4m3_terms
 from . import fp4_codec
 
 D_LATENT = 512
@@ -114,6 +114,22 @@ def mla_decode(q_abs: np.ndarray, q_rope: np.ndarray, rows: np.ndarray,
         g = gather_rows(rows, block_table[b], n)
         out[b, i], lse[b, i] = attend_latent(q_abs[b, i], q_rope[b, i], g, scale)
     return out, lse
+
+
+def query_as_e4m3_terms(q_abs: np.ndarray, q_rope: np.ndarray, terms: int = 2):
+    """The query a block-scaled FP8 score product would see.
+
+    Each head's 576-value row [q_abs | q_rope] is split into e4m3 terms with
+    one e8m0 scale per 32 values (fp8_codec.split_e4m3_terms: the scale
+    groups are the cache row's, so group k of the query meets group k of
+    the key).  terms=1 keeps the first term alone, terms=2 their sum.
+    Returns the float64 value, split back into its 512 and 64 parts; decoding
+    with it is mla_decode / attend_latent on these arrays.
+    """
+    q = np.concatenate([np.asarray(q_abs, dtype=np.float64), np.asarray(q_rope, dtype=np.float64)], axis=-1)
+    hi, lo = split_e4m3_terms(q)
+    v = dequant_blocks(*hi) + (dequant_blocks(*lo) if terms == 2 else 0.0)
+    return v[..., :D_LATENT], v[..., D_LATENT:]
 
 
 def merge_partials(outs: np.ndarray, lses: np.ndarray):
