@@ -37,6 +37,54 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(declared_functions()) <= set(binding.SIGNATURES)
 
 
+def _declarations():
+    """name -> (return type, [argument types]) from the header's prototypes."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"([A-Za-z_][A-Za-z0-9_ *]*?)\b(mla_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        args = [" ".join(a.split()) for a in m.group(3).split(",")] if m.group(3).strip() else []
+        # drop each argument's name, keep its type (with any '*')
+        types = [re.sub(r"\s*\b[A-Za-z_][A-Za-z0-9_]*$", "", a).replace(" *", "*") for a in args]
+        out[m.group(2)] = (" ".join(m.group(1).split()).replace(" *", "*"), types)
+    return out
+
+
+def _ctype_of(c_type):
+    c_type = c_type.replace("const ", "")
+    if c_type == "int":
+        return ctypes.c_int
+    if c_type == "float":
+        return ctypes.c_float
+    if c_type == "size_t":
+        return ctypes.c_size_t
+    if c_type == "size_t*":
+        return ctypes.POINTER(ctypes.c_size_t)
+    if c_type == "char*":
+        return ctypes.c_char_p
+    if c_type.endswith("*"):
+        return ctypes.c_void_p
+    raise AssertionError("unmapped C type " + c_type)
+
+
+def test_binding_signatures_match_the_header_argument_by_argument():
+    decls = _declarations()
+    assert set(decls) == set(binding.SIGNATURES)
+    for name, (ret, args) in decls.items():
+        res, argtypes = binding.SIGNATURES[name]
+        assert res is _ctype_of(ret), name
+        assert len(argtypes) == len(args), name
+        for i, (want, got) in enumerate(zip(args, argtypes)):
+            w = _ctype_of(want)
+            same = got is w or (hasattr(w, "_type_") and getattr(got, "_type_", None) is w._type_)
+            assert same, (name, i, want, got)
+
+
+def test_status_codes_match_the_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    codes = {int(v): k for k, v in re.findall(r"\b(MLA_[A-Z_]+)\s*=\s*(-?\d+)", text)}
+    assert codes == binding._STATUS
+
+
 def test_status_strings(lib):
     for code, name in binding._STATUS.items():
         assert lib.mla_status_string(code).decode() == name
