@@ -460,6 +460,8 @@ def run_ours(args):
     roof["roofline_frac_of_call"] = max(t_bytes, t_flop) / (ms_per_step / 1000.0)
     roof["hbm_gbs"] = gbs
     roof["tflops"] = tfs
+    # the tensor pipe's share against the power-capped (sustained) GEMM rate
+    roof["tensor_frac_of_sustained"] = tfs / peaks["bf16_sus"]
 
     # ---- end to end through the public API with pinned host buffers.
     # Every step uploads its inputs and reads its outputs back, pipelined the
