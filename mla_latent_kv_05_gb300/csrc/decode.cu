@@ -12,7 +12,8 @@
 // is computed twice:
 //   rank 1 ("score SM"): Q [128 x 576] bf16 resident in TMEM (288 columns);
 //       per tile of N tokens S = Q . K^T (36 tcgen05.mma, M=128, A from TMEM)
-//       into one of two N-column S buffers; eight softmax warps in two groups
+//       into one of two N-column S buffers (three for the quantised caches);
+//       eight softmax warps in two groups
 //       (each turns half of the tile's columns into P, both take the row max
 //       over all N columns, so their reference maxima agree without an
 //       exchange) round P to bf16 and send it with st.async into rank 0's
@@ -22,7 +23,8 @@
 //       O += P . V with P from shared memory and V read as an MN-major operand
 //       (two M=128, N=256, K=16 MMAs per 16 tokens); its epilogue warps
 //       rescale O when rank 1 moves a head's reference max and write
-//       out = O / l (or an fp32 split partial).
+//       out = O / l (or, for a row split over several pairs, the bf16
+//       partial that the merge kernel combines).
 //
 // Tiles of 96 tokens.  A tcgen05.mma with N <= 96 costs about as much as one
 // with N = 64, so the score SM works on 96-token tiles (three half pages).
@@ -47,6 +49,8 @@
 // dequantises what its own MMAs read (score SM: all nine chunks into the
 // nine-chunk K layout; value SM: the eight latent chunks into V slots), in
 // 64-token tiles (the raw buffers take the shared memory of a third slot).
+// The FP4 cache and the V4.1 rows (528-byte FP8, 288-byte FP4) use the same
+// roles, layouts and tiles with their own raw copies and decoders.
 // Moving dequantised rows between the two SMs would cost more than the
 // second dequant: traffic inside a cluster runs at about 42 GB/s per pair.
 //
