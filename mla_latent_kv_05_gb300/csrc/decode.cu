@@ -531,7 +531,9 @@ __device__ __forceinline__ void load_q_rolled(const uint8_t* qa, const uint8_t* 
 // kMode 0: bf16 cache via TMA; 1: FP8 cache via bulk copies + dequant to
 // bf16 operands; 2: FP8 cache with f16 operands (flags inputs outside the
 // f16-exact range, which mode 1 then recomputes); 3: sparse top-k decode
-// over the bf16 cache (rows gathered by listed slot with 16-byte cp.async)
+// over the bf16 cache (rows gathered by listed slot with 16-byte cp.async);
+// 4 / 5: the FP4 cache as 1 / 2; 6 / 7: the 528-byte V4.1 FP8 rows as 1 / 2;
+// 8 / 9: the 288-byte V4.1 FP4 rows as 1 / 2
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dk::Cfg<kMode>::kThreads, 1)
 mla_decode_pair_kernel(const __grid_constant__ CacheMaps maps, const DecodeParams p) {
