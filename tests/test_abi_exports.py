@@ -134,3 +134,34 @@ def test_sparse_host_validation_without_gpu(lib):
     rc = lib.mla_decode_sparse_bf16(fake, fake, fake, fake, 1, 1, 64, 128, 8, 64, ctypes.c_float(float("inf")),
                                     fake, fake, fake, 1 << 30, z)
     assert rc == -1
+
+
+DENSE_ENTRIES = ["mla_decode_bf16", "mla_decode_fp8", "mla_decode_fp4", "mla_decode_fp8_v41", "mla_decode_fp4_v41"]
+
+
+@pytest.mark.parametrize("name", DENSE_ENTRIES)
+def test_every_dense_entry_validates_on_the_host(lib, name):
+    """Each dense decode entry checks its arguments before touching CUDA:
+    the same codes from every cache format."""
+    fn = getattr(lib, name)
+    z = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+
+    def call(q=fake, cache=fake, batch=1, sq=1, heads=128, pages=8, page=64, max_pages=4, scale=0.1, ws=fake):
+        return fn(q, fake, cache, fake, fake, batch, sq, heads, pages, page, max_pages, ctypes.c_float(scale),
+                  fake, fake, ws, 1 << 30, z)
+
+    assert call(q=z) == -1                                   # null pointer
+    assert call(ws=z) == -1
+    assert call(batch=-1) == -1
+    assert call(sq=0) == -1
+    assert call(max_pages=0) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(scale=0.0) == -1
+    assert call(cache=ctypes.c_void_p(0x1008)) == -1         # cache not 16-byte aligned
+    assert call(ws=ctypes.c_void_p(0x1080)) == -1            # workspace not 256-byte aligned
+    assert call(heads=64) == -2
+    assert call(page=32) == -2
+    assert call(sq=5) == -2
+    assert call(batch=1 << 15, sq=4) == -2                   # more query rows than the planner takes
+    assert call(batch=0) == 0                                # nothing to do: returns before any launch
