@@ -165,3 +165,25 @@ def test_every_dense_entry_validates_on_the_host(lib, name):
     assert call(sq=5) == -2
     assert call(batch=1 << 15, sq=4) == -2                   # more query rows than the planner takes
     assert call(batch=0) == 0                                # nothing to do: returns before any launch
+
+
+def test_up_projection_merge_and_profiling_entries_validate_on_the_host(lib):
+    z = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+    wuv = lib.mla_up_project_wuv
+    assert wuv(z, fake, 4, 128, 128, fake, fake, 1 << 20, z) == -1          # null latent
+    assert wuv(fake, fake, -1, 128, 128, fake, fake, 1 << 20, z) == -1      # negative rows
+    assert wuv(fake, fake, 4, 64, 128, fake, fake, 1 << 20, z) == -2        # num_heads != 128
+    assert wuv(fake, fake, 4, 128, 64, fake, fake, 1 << 20, z) == -2        # d_v != 128
+    assert wuv(fake, fake, (1 << 16) + 1, 128, 128, fake, fake, 1 << 20, z) == -2
+    assert wuv(fake, ctypes.c_void_p(0x1002), 4, 128, 128, fake, fake, 1 << 20, z) == -1   # W^UV not 16-byte aligned
+    assert wuv(fake, fake, 4, 128, 128, fake, fake, 8, z) == -3             # workspace smaller than its header
+    assert wuv(fake, fake, 0, 128, 128, fake, fake, 1 << 20, z) == 0        # no rows: nothing launched
+    comb = lib.mla_combine_splits
+    assert comb(fake, fake, fake, 3, 64, fake, fake, z) == -2               # num_heads != 128
+    assert comb(z, fake, fake, 3, 128, fake, fake, z) == -1                 # null partials
+    assert comb(ctypes.c_void_p(0x1004), fake, fake, 3, 128, fake, fake, z) == -1
+    assert comb(z, z, fake, 0, 128, fake, fake, z) == 0                     # no rows
+    assert lib.mla_profile_next_decode(fake, z) == -1                       # both events or neither
+    assert lib.mla_profile_next_decode(z, z) == 0
+    assert lib.mla_get_status(z, z) == -1
