@@ -50,6 +50,13 @@
  * for its predecessor (griddepcontrol.wait) before reading out or lse, as
  * programmatic dependent launch requires of any kernel.
  *
+ * Threads and devices: every call works on the calling thread's current
+ * CUDA device.  The first call on a device sets the kernels' shared-memory
+ * limits and caches the number of resident CTA pairs in process-wide
+ * variables that take no lock, so make the first call on each device from
+ * one thread; later calls may come from any thread, each with its own
+ * stream and workspace (mla_profile_next_decode is per thread).
+ *
  * Errors: host-side validation failures return a negative mla_status before
  * anything is launched.  Launch failures return MLA_ERR_CUDA.  Problems only
  * the device can see (a block-table entry outside [0, num_pages), a
