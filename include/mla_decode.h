@@ -262,6 +262,9 @@ int mla_up_project_wuv(const uint16_t* latent, const uint16_t* w_uv, int rows, i
  * partial_out [n_parts, num_heads, 512] fp32 (each part already normalised
  * by its own softmax sum), partial_lse [n_parts, num_heads] fp32,
  * split_indptr [rows+1] int32: row r merges parts [indptr[r], indptr[r+1]).
+ * The call has no n_parts argument and reads the parts split_indptr names
+ * without a bound: it must start at 0, never decrease and end at most at
+ * n_parts (device memory, so the host cannot check it).
  * A row with no part (or whose parts all have lse = -inf) gets out = 0,
  * lse = -inf.  out [rows, num_heads, 512] bf16, lse [rows, num_heads] fp32.
  * num_heads must be 128. */

@@ -109,6 +109,20 @@ def _check(t: torch.Tensor, name: str, dtype, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _same_device(tensors: dict, current: int) -> None:
+    """Every tensor of a call on one CUDA device, the calling thread's current
+    one: the library launches its kernels on the current device, which then
+    reads and writes these pointers."""
+    devs = {name: t.device for name, t in tensors.items() if t is not None}
+    first_name, first = next(iter(devs.items()))
+    for name, d in devs.items():
+        if d != first:
+            raise ValueError(f"{name} is on {d} but {first_name} is on {first}")
+    if first.index != current:
+        raise ValueError(f"the tensors are on {first} but the current device is cuda:{current}; "
+                         f"call under torch.cuda.device({first})")
+
+
 def mla_workspace_size(batch: int, sq: int, num_heads: int = 128, page_size: int = 64) -> int:
     n = ctypes.c_size_t(0)
     rc = load().mla_workspace_size(int(batch), int(sq), int(num_heads), int(page_size), ctypes.byref(n))
@@ -144,6 +158,8 @@ def _decode(fn_name, q_absorbed, q_rope, kv_cache, block_table, seq_lens, scale,
     if workspace is None:
         workspace = alloc_workspace(B, Sq, q_absorbed.device)
     _check(workspace, "workspace", torch.uint8)
+    _same_device(dict(q_absorbed=q_absorbed, q_rope=q_rope, kv_cache=kv_cache, block_table=block_table,
+                      seq_lens=seq_lens, out=out, lse=lse, workspace=workspace), torch.cuda.current_device())
     rc = getattr(load(), fn_name)(
         _ptr(q_absorbed), _ptr(q_rope), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
         int(B), int(Sq), int(H), int(kv_cache.shape[0]), int(kv_cache.shape[1]), int(block_table.shape[1]),
@@ -186,6 +202,9 @@ def mla_decode_bf16_noalloc(q_absorbed, q_rope, kv_cache, block_table, seq_lens,
     _check(lse, "lse", torch.float32, (B, Sq, H))
     if device_status is not None:
         _check(device_status, "device_status", torch.int32, (1,))
+    _same_device(dict(q_absorbed=q_absorbed, q_rope=q_rope, kv_cache=kv_cache, block_table=block_table,
+                      seq_lens=seq_lens, out=out, lse=lse, device_status=device_status),
+                 torch.cuda.current_device())
     rc = load().mla_decode_bf16_noalloc(
         _ptr(q_absorbed), _ptr(q_rope), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
         int(B), int(Sq), int(H), int(kv_cache.shape[0]), int(kv_cache.shape[1]), int(block_table.shape[1]),
@@ -273,6 +292,8 @@ def mla_decode_sparse_bf16(q_absorbed, q_rope, kv_cache, token_slots, scale, out
     if workspace is None:
         workspace = alloc_workspace_sparse(B, Sq, topk, q_absorbed.device)
     _check(workspace, "workspace", torch.uint8)
+    _same_device(dict(q_absorbed=q_absorbed, q_rope=q_rope, kv_cache=kv_cache, token_slots=token_slots, out=out,
+                      lse=lse, workspace=workspace), torch.cuda.current_device())
     rc = load().mla_decode_sparse_bf16(
         _ptr(q_absorbed), _ptr(q_rope), _ptr(kv_cache), _ptr(token_slots), int(B), int(Sq), topk, int(H),
         int(kv_cache.shape[0]), int(kv_cache.shape[1]), ctypes.c_float(float(scale)), _ptr(out), _ptr(lse),
@@ -299,6 +320,7 @@ def mla_up_project_wuv(latent, w_uv, out=None, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.zeros(256, dtype=torch.uint8, device=latent.device)
     _check(workspace, "workspace", torch.uint8)
+    _same_device(dict(latent=latent, w_uv=w_uv, out=out, workspace=workspace), torch.cuda.current_device())
     rc = load().mla_up_project_wuv(_ptr(latent), _ptr(w_uv), rows, 128, 128, _ptr(out), _ptr(workspace),
                                    ctypes.c_size_t(workspace.numel()), _stream(stream))
     if rc != MLA_OK:
@@ -310,14 +332,22 @@ def mla_combine_splits(partial_out, partial_lse, split_indptr, out=None, lse=Non
     """Merge split partials: partial_out [n, 128, 512] fp32, partial_lse [n, 128] fp32,
     split_indptr [rows+1] int32 -> (out [rows, 128, 512] bf16, lse [rows, 128] fp32)."""
     _check(partial_out, "partial_out", torch.float32)
-    _check(partial_lse, "partial_lse", torch.float32)
+    if partial_out.dim() != 3 or partial_out.shape[2] != 512:
+        raise ValueError(f"partial_out must be [n_parts, num_heads, 512], got {tuple(partial_out.shape)}")
+    _check(partial_lse, "partial_lse", torch.float32, tuple(partial_out.shape[:2]))
     _check(split_indptr, "split_indptr", torch.int32)
+    if split_indptr.dim() != 1 or split_indptr.numel() < 1:
+        raise ValueError("split_indptr must be [rows + 1]")
     rows = split_indptr.numel() - 1
     H = partial_out.shape[1]
     if out is None:
         out = torch.empty((rows, H, 512), dtype=torch.bfloat16, device=partial_out.device)
     if lse is None:
         lse = torch.empty((rows, H), dtype=torch.float32, device=partial_out.device)
+    _check(out, "out", torch.bfloat16, (rows, H, 512))
+    _check(lse, "lse", torch.float32, (rows, H))
+    _same_device(dict(partial_out=partial_out, partial_lse=partial_lse, split_indptr=split_indptr, out=out, lse=lse),
+                 torch.cuda.current_device())
     rc = load().mla_combine_splits(_ptr(partial_out), _ptr(partial_lse), _ptr(split_indptr), int(rows), int(H),
                                    _ptr(out), _ptr(lse), _stream(stream))
     if rc != MLA_OK:
