@@ -92,6 +92,42 @@ def test_fp8_row_dequant_layout_against_torch():
     assert np.array_equal(as_bf16, mine)
 
 
+def _fp8_pins_ok(decode) -> bool:
+    """The 594-byte row against torch's float8 casts, for a candidate decoder."""
+    raw = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp8", seed=3).kv_cache
+    v = raw[..., :576].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    s = fp8_codec.e8m0_to_float64(raw[..., 576:].numpy())      # pinned against torch's e8m0 cast above
+    ref = v.numpy() * np.repeat(s, 32, axis=-1)
+    return np.array_equal(decode(raw.numpy()), ref)
+
+
+def test_fp8_pins_catch_planted_mistakes():
+    good = fp8_codec.dequant_rows
+    assert _fp8_pins_ok(good)
+
+    def scales_one_byte_late(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., 576:] = np.roll(raw[..., 576:], 1, axis=-1)
+        return good(raw)
+
+    def scale_per_16(raw):
+        raw = np.asarray(raw)
+        vals = fp8_codec.e4m3fn_to_float64(raw[..., :576])
+        sc = fp8_codec.e8m0_to_float64(raw[..., 576:])
+        return vals * sc[..., (np.arange(576) // 16) % 18]
+
+    def e8m0_bias_126(raw):
+        return good(raw) * 2.0
+
+    def rope_unscaled(raw):
+        out = good(raw)
+        out[..., 512:] = fp8_codec.e4m3fn_to_float64(np.asarray(raw)[..., 512:576])
+        return out
+
+    for bad in (scales_one_byte_late, scale_per_16, e8m0_bias_126, rope_unscaled):
+        assert not _fp8_pins_ok(bad), bad.__name__
+
+
 def test_v41_row_is_the_printed_528_bytes():
     # "DeepSeek-R1" record, constraint (2): 512 e4m3 values plus 16 e8m0
     # scales, one per 32 values, make the 528-byte V4.1 row
@@ -247,6 +283,49 @@ def test_fp4_value_k_takes_scale_k_div_16():
     sc = raw[..., 288:].astype(np.int64)
     for k in (0, 15, 16, 31, 100, 511, 512, 575):
         assert np.array_equal(v[..., k], np.exp2(sc[..., k // 16] - 127.0)), k
+
+
+def _fp4_pins_ok(decode) -> bool:
+    """The by-hand 324-byte row and the per-16 scale rule, for a candidate
+    decoder [..., 324] -> [..., 576]."""
+    row = np.zeros(324, dtype=np.uint8)
+    row[0], row[7], row[8], row[287] = 0x21, 0xF7, 0x3B, 0x5C
+    row[288], row[289], row[323] = 127, 130, 125
+    v = decode(row)
+    if not ((v[0], v[1], v[14], v[15], v[16], v[17], v[574], v[575]) ==
+            (0.5, 1.0, 6.0, -6.0, -12.0, 12.0, -0.5, 0.75) and np.count_nonzero(v) == 8):
+        return False
+    raw = gen.make_inputs(1, 1, [64], kv_dtype="fp4", seed=9).kv_cache.numpy().copy()
+    raw[..., :288] = 0x22
+    v = decode(raw)
+    sc = raw[..., 288:].astype(np.int64)
+    return all(np.array_equal(v[..., k], np.exp2(sc[..., k // 16] - 127.0)) for k in range(576))
+
+
+def test_fp4_pins_catch_planted_mistakes():
+    good = fp4_codec.dequant_rows
+    assert _fp4_pins_ok(good)
+
+    def nibbles_swapped(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., :288] = ((raw[..., :288] & 0x0F) << 4) | (raw[..., :288] >> 4)
+        return good(raw)
+
+    def one_scale_per_32(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., 288:] = np.repeat(raw[..., 288:306], 2, axis=-1)
+        return good(raw)
+
+    def scales_one_byte_late(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., 288:] = np.roll(raw[..., 288:], 1, axis=-1)
+        return good(raw)
+
+    def sign_dropped(raw):
+        return np.abs(good(raw))
+
+    for bad in (nibbles_swapped, one_scale_per_32, scales_one_byte_late, sign_dropped):
+        assert not _fp4_pins_ok(bad), bad.__name__
 
 
 def test_fp4_generated_rows_are_bf16_exact():
