@@ -468,6 +468,49 @@ def test_split_merge_equals_unsplit():
     np.testing.assert_allclose(o, full, rtol=1e-13)
 
 
+def _merge_pins_ok(merge) -> bool:
+    """Split + merge reproduces the unsplit attention, and an all-empty row
+    merges to 0 and -inf, for a candidate merge (outs [k,H,D], lses [k,H])."""
+    rng = np.random.default_rng(4)
+    rows = rng.standard_normal((300, 576))
+    qa, qr = rng.standard_normal((16, 512)), rng.standard_normal((16, 64))
+    full, lse_full = mla_oracle.attend_latent(qa, qr, rows, 0.07)
+    cuts = [0, 1, 64, 65, 299, 300]
+    parts = [mla_oracle.attend_latent(qa, qr, rows[a:b], 0.07) for a, b in zip(cuts[:-1], cuts[1:])]
+    with np.errstate(all="ignore"):
+        o, l = merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        if not (np.allclose(o, full, rtol=1e-10, atol=1e-12) and np.allclose(l, lse_full, rtol=1e-12)):
+            return False
+        e = mla_oracle.attend_latent(qa, qr, rows[:0], 0.07)
+        o, l = merge(np.stack([e[0], e[0]]), np.stack([e[1], e[1]]))
+    return bool(np.all(o == 0) and np.all(np.isneginf(l)))
+
+
+def test_merge_pins_catch_planted_mistakes():
+    good = mla_oracle.merge_partials
+    assert _merge_pins_ok(good)
+
+    def base2_lse(outs, lses):
+        o, l = good(outs, lses)
+        return o, np.logaddexp2.reduce(np.asarray(lses), axis=0)
+
+    def plain_average(outs, lses):
+        o, l = good(outs, lses)
+        return np.mean(np.asarray(outs), axis=0), l
+
+    def weights_not_normalised(outs, lses):
+        lses = np.asarray(lses)
+        return np.einsum("kh,khd->hd", np.exp(lses), np.asarray(outs)), np.logaddexp.reduce(lses, axis=0)
+
+    def empty_row_nan(outs, lses):
+        lses = np.asarray(lses)
+        L = np.logaddexp.reduce(lses, axis=0)
+        return np.einsum("kh,khd->hd", np.exp(lses - L), np.asarray(outs)), L
+
+    for bad in (base2_lse, plain_average, weights_not_normalised, empty_row_nan):
+        assert not _merge_pins_ok(bad), bad.__name__
+
+
 def test_causal_two_token_query():
     inp = gen.make_inputs(2, 2, [65, 1], seed=9)
     rows = mla_oracle.cache_rows(_f64(inp.kv_cache), "bf16")
