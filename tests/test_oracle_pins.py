@@ -527,6 +527,39 @@ def test_causal_two_token_query():
             np.testing.assert_allclose(lse[b, i], rl, rtol=1e-12)
 
 
+def _causal_pin_ok() -> bool:
+    """Sq = 2 and 3 query blocks: query i sees seq_len - (Sq-1-i) tokens,
+    counted here by hand, each row checked against torch's SDPA."""
+    for sq, lens in ((2, [65, 1]), (3, [130, 2])):
+        inp = gen.make_inputs(2, sq, lens, seed=9)
+        rows = mla_oracle.cache_rows(_f64(inp.kv_cache), "bf16")
+        qa, qr = _f64(inp.q_absorbed), _f64(inp.q_rope)
+        out, lse = mla_oracle.mla_decode(qa, qr, rows, inp.block_table.numpy(), inp.seq_lens.numpy(), inp.scale)
+        for b, s in enumerate(lens):
+            for i in range(sq):
+                n = max(s - (sq - 1 - i), 0)
+                if n == 0:
+                    if not (np.all(out[b, i] == 0) and np.all(lse[b, i] == -np.inf)):
+                        return False
+                    continue
+                g = mla_oracle.gather_rows(rows, inp.block_table[b].numpy(), n)
+                ro, rl = _sdpa_reference(qa[b, i], qr[b, i], g, inp.scale)
+                if not (np.allclose(out[b, i], ro, rtol=1e-11, atol=1e-12) and np.allclose(lse[b, i], rl, rtol=1e-12)):
+                    return False
+    return True
+
+
+def test_causal_pin_catches_planted_mistakes(monkeypatch):
+    assert _causal_pin_ok()
+    for bad in (lambda s, sq, i: int(s) - (int(sq) - int(i)),      # one token short everywhere
+                lambda s, sq, i: int(s) - int(i),                   # the query order reversed
+                lambda s, sq, i: int(s)):                           # no causal rule
+        monkeypatch.setattr(mla_oracle, "visible_len", bad)
+        assert not _causal_pin_ok()
+    monkeypatch.undo()
+    assert _causal_pin_ok()
+
+
 def _pin_suite(attend):
     """Run the attention pins against a candidate implementation; return the
     number of pins that fail."""
