@@ -13,7 +13,8 @@ clocks sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..9]
   (workloads 1..5: the dense configurations; 6: sparse top-2048 decode;
-  7: the FP4 cache at the FP8 workload's shape)
+  7: the FP4 cache at the FP8 workload's shape; 8 and 9: the V4.1 FP8 and
+  FP4 rows at that shape)
   python bench.py --impl reference ...   # the oracle arm (host cores)
 """
 from __future__ import annotations
