@@ -70,3 +70,46 @@ def test_counts_per_cache_format():
         assert c["kv_bytes"] == 128 * row, kv
     assert gen.WORKLOADS[7]["kv_dtype"] == "fp4"
     assert gen.WORKLOADS[7]["batch"] == gen.WORKLOADS[4]["batch"] and gen.WORKLOADS[7]["seq"] == gen.WORKLOADS[4]["seq"]
+
+
+def test_v41_caches_bytes_scales_and_counts():
+    a = gen.make_inputs(2, 1, [100, 3], kv_dtype="fp8v41", seed=1)
+    assert a.kv_cache.shape == (3, 64, 528) and a.kv_cache.dtype == torch.uint8
+    sc = a.kv_cache[..., 512:]
+    assert int(sc.min()) >= 120 and int(sc.max()) <= 130
+    assert torch.isfinite(a.kv_cache[..., :512].contiguous().view(torch.float8_e4m3fn).float()).all()
+    b = gen.make_inputs(2, 1, [100, 3], kv_dtype="fp4v41", seed=1)
+    assert b.kv_cache.shape == (3, 64, 288)
+    assert int(b.kv_cache[..., 256:].min()) >= 120 and int(b.kv_cache[..., 256:].max()) <= 130
+    # the V4.1 rows' FLOPs are counted on their own 448-value latent
+    for kv, row in (("fp8v41", 528), ("fp4v41", 288)):
+        c = gen.workload_counts(gen.make_inputs(2, 1, [100, 28], kv_dtype=kv, seed=0))
+        assert c["kv_bytes"] == 128 * row
+        assert c["flops"] == 128 * 2 * 128 * ((448 + 64) + 448)
+    for w in (8, 9):
+        assert gen.WORKLOADS[w]["batch"] == 128 and gen.WORKLOADS[w]["seq"] == 8192
+
+
+def test_workload3_lengths_are_the_seeded_uniform_draw():
+    lens = gen.workload_seq_lens(3)
+    assert lens == gen.workload_seq_lens(3) and len(lens) == 64
+    assert min(lens) >= 1 and max(lens) <= 32768
+    assert 8000 < sum(lens) / 64 < 24000                       # a U[1, 32768] mean, loosely
+    assert gen.workload_seq_lens(2) == [4096] * 32
+
+
+def test_sparse_lists_name_distinct_visible_slots():
+    sp = gen.make_sparse_inputs(3, 2, [300, 5, 0], 64, seed=2, pad_middle=True)
+    bt = sp.dense.block_table
+    for b, ctx in enumerate([300, 5, 0]):
+        for i in range(2):
+            vis = max(ctx - (1 - i), 0)
+            lst = [int(x) for x in sp.token_slots[b, i] if int(x) >= 0]
+            assert len(lst) == len(set(lst)) <= min(vis, 64)
+            allowed = {int(bt[b, t // 64]) * 64 + t % 64 for t in range(vis)}
+            assert set(lst) <= allowed
+            if not sp.token_slots.shape[2] > vis:
+                continue
+            assert (sp.token_slots[b, i] == -1).sum() >= 64 - vis
+    c = gen.sparse_counts(sp)
+    assert c["kv_tokens"] == int((sp.token_slots >= 0).sum())
