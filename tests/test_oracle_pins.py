@@ -247,6 +247,48 @@ def test_v41_pins_catch_planted_mistakes():
         assert not _v41_fp8_pins_ok(bad), bad.__name__
 
 
+def _v41_fp4_pins_ok(decode) -> bool:
+    """The 288-byte row's hand-built pin and its 324-byte embedding, for a
+    candidate decoder [..., 288] -> [..., 576]."""
+    row = np.zeros(288, dtype=np.uint8)
+    row[:256] = 0x22
+    row[256:] = 117 + np.arange(32)
+    v = 2.0 ** (np.arange(512) // 16 - 10)
+    want = np.zeros(576)
+    want[:448], want[512:] = v[:448], v[448:]
+    if not np.array_equal(decode(row), want):
+        return False
+    raw = gen.make_inputs(2, 1, [70, 5], kv_dtype="fp4v41", seed=6).kv_cache.numpy()
+    wide = np.zeros(raw.shape[:-1] + (324,), dtype=np.uint8)
+    wide[..., :224], wide[..., 256:288] = raw[..., :224], raw[..., 224:256]
+    wide[..., 288:316], wide[..., 316:320], wide[..., 320:324] = raw[..., 256:284], 127, raw[..., 284:288]
+    return np.array_equal(decode(raw), fp4_codec.dequant_rows(wide))
+
+
+def test_fp4_v41_pins_catch_planted_mistakes():
+    good = fp4_codec.dequant_rows_v41
+    assert _v41_fp4_pins_ok(good)
+
+    def scales_one_group_late(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., 256:] = np.roll(raw[..., 256:], 1, axis=-1)
+        return good(raw)
+
+    def rope_in_the_padding(raw):
+        out = good(raw)
+        fixed = out.copy()
+        fixed[..., 448:512], fixed[..., 512:] = out[..., 512:], 0
+        return fixed
+
+    def nibbles_swapped(raw):
+        raw = np.asarray(raw).copy()
+        raw[..., :256] = ((raw[..., :256] & 0x0F) << 4) | (raw[..., :256] >> 4)
+        return good(raw)
+
+    for bad in (scales_one_group_late, rope_in_the_padding, nibbles_swapped):
+        assert not _v41_fp4_pins_ok(bad), bad.__name__
+
+
 def test_e2m1_table_is_the_ocp_value_set():
     # OCP MX FP4 E2M1: the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 in
     # code order, the sign bit negating them; no NaN or infinity
