@@ -444,6 +444,52 @@ def test_absorption_identity():
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-12)
 
 
+def _absorption_ok(attend_unabsorbed, up_project) -> bool:
+    """The absorption identity for candidate un-absorbed attention and
+    up-projection, against the SDPA-pinned latent form."""
+    rng = np.random.default_rng(15)
+    H, d_h, n = 8, 128, 61
+    w_uk = rng.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    w_uv = rng.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    q_nope, q_rope = rng.standard_normal((H, d_h)), rng.standard_normal((H, 64))
+    c_kv, k_r = rng.standard_normal((n, 512)), rng.standard_normal((n, 64))
+    scale = 1 / math.sqrt(192)
+    try:
+        o_ref, lse_ref = attend_unabsorbed(q_nope, q_rope, c_kv, k_r, w_uk, w_uv, scale)
+        out_lat, lse = mla_oracle.attend_latent(mla_oracle.absorb_query(q_nope, w_uk), q_rope,
+                                                np.concatenate([c_kv, k_r], 1), scale)
+        o = up_project(out_lat, w_uv)
+    except (ValueError, IndexError):
+        return False
+    return bool(np.allclose(o, o_ref, rtol=1e-10, atol=1e-12) and np.allclose(lse, lse_ref, rtol=1e-12))
+
+
+def test_absorption_pins_catch_planted_mistakes():
+    good_attend, good_up = mla_oracle.attend_unabsorbed, mla_oracle.up_project_output
+    assert _absorption_ok(good_attend, good_up)
+
+    def values_through_w_uk(q_nope, q_rope, c_kv, k_r, w_uk, w_uv, scale):
+        return good_attend(q_nope, q_rope, c_kv, k_r, w_uk, w_uk, scale)
+
+    def rope_dropped(q_nope, q_rope, c_kv, k_r, w_uk, w_uv, scale):
+        return good_attend(q_nope, np.zeros_like(q_rope), c_kv, k_r, w_uk, w_uv, scale)
+
+    def heads_shifted(q_nope, q_rope, c_kv, k_r, w_uk, w_uv, scale):
+        return good_attend(q_nope, q_rope, c_kv, k_r, w_uk, np.roll(w_uv, 1, axis=0), scale)
+
+    for bad in (values_through_w_uk, rope_dropped, heads_shifted):
+        assert not _absorption_ok(bad, good_up), bad.__name__
+
+    def up_transposed(out_lat, w_uv):
+        return np.einsum("hck,hc->hk", w_uv.transpose(0, 2, 1), out_lat[:, :128])
+
+    def up_first_head_only(out_lat, w_uv):
+        return np.einsum("kc,hc->hk", w_uv[0], out_lat)
+
+    for bad in (up_transposed, up_first_head_only):
+        assert not _absorption_ok(good_attend, bad), bad.__name__
+
+
 def test_single_token_is_exact_row():
     rng = np.random.default_rng(1)
     row = rng.standard_normal((1, 576))
