@@ -300,8 +300,35 @@ def run_reference(args):
                          "sample": f"per step: {desc}; ~{per_step}s of host work"},
         "e2e": {"value": value, "unit": "KV-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if args.workload == 1:
+        line["cpu_baseline"]["unabsorbed"] = unabsorbed_sample(inp)
     print(json.dumps(line))
     return 0
+
+
+def unabsorbed_sample(inp) -> dict:
+    """The oracle's un-absorbed form (explicit per-head W^UK and W^UV, seeded
+    N(0,1)/sqrt(512) weights, d_h = 128) on the oracle-sized workload's one
+    query row, beside the absorbed form on the same row: what absorption
+    saves on the host."""
+    from oracle import mla_oracle
+    rng = np.random.default_rng(7)
+    H, d_h = int(inp.q_absorbed.shape[2]), 128
+    n = int(inp.seq_lens[0])
+    w_uk = rng.standard_normal((H, d_h, 512)) / np.sqrt(512)
+    w_uv = rng.standard_normal((H, d_h, 512)) / np.sqrt(512)
+    q_nope = rng.standard_normal((H, d_h))
+    rows = mla_oracle.cache_rows(inp.kv_cache.double().numpy(), "bf16")
+    g = mla_oracle.gather_rows(rows, inp.block_table[0].numpy(), n)
+    qr = inp.q_rope[0, 0].double().numpy()
+    t0 = time.perf_counter()
+    mla_oracle.attend_unabsorbed(q_nope, qr, g[:, :512], g[:, 512:], w_uk, w_uv, inp.scale)
+    t_un = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    mla_oracle.attend_latent(mla_oracle.absorb_query(q_nope, w_uk), qr, g, inp.scale)
+    t_abs = time.perf_counter() - t0
+    return {"value": n / t_un, "unit": "KV-tokens/s", "absorbed_value": n / t_abs,
+            "sample": f"one query row, {H} heads, {n} tokens; absorbed form on the same row for comparison"}
 
 
 # ----------------------------------------------------------------- GPU arm
